@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Benchmark of the CacheGen codec's hot path on GB300.
+
+One step = encode + decode of one synthetic KV blob that is already in HBM
+(quantise, histograms/CDFs, arithmetic coding, packing; then prefix-sum
+decoding with fused dequantisation). The metric is GB/s of raw bf16 KV per
+step; encode and decode GB/s, the compression ratio, the dominant kernel's
+HBM roofline fraction, an end-to-end figure through host buffers, and the
+CPU oracle's speed on the host cores are reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Under torchrun (N > 1) every rank encodes and decodes its own replica of
+the workload (weak scaling; the codec has no exchange step), the ranks
+barrier around the timed region, and rank 0 reports the slowest rank's
+time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CacheGen encode+decode throughput (GB/s of raw bf16 KV)"
+DEFAULT_WORKLOAD = "llama8b_t16k"
+KERNEL_SOURCE = os.path.join(ROOT, "kv_cache_compression_03_gb300", "csrc", "cachegen_kernels.cu")
+
+
+# ----------------------------------------------------------------- ranks
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate_max(value: float, world: int, backend_device=None) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=backend_device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while it runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 20):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workload
+
+def workload_info(name: str):
+    from kv_cache_compression_03_gb300 import synthetic
+    p = synthetic.WORKLOADS[name]
+    k, v = synthetic.workload_specs(name)
+    return p, k, v
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("source_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(name: str, bits):
+    """Encode + decode a bounded sample (bits = the first tokens of the
+    workload) with the CPU oracle on all host cores. Returns (seconds, raw
+    bytes, threads, encoded)."""
+    from oracle import oracle
+    p, k, v = workload_info(name)
+    L, _, T, C = bits.shape
+    ch = p["chunk_tokens"][0]
+    nth = oracle.max_threads()
+    t0 = time.perf_counter()
+    enc = oracle.encode(bits, ch, k, v, nthreads=nth)
+    oracle.decode(enc, L, T, C, ch, k, v, nthreads=nth)
+    dt = time.perf_counter() - t0
+    return dt, bits.nbytes, nth, enc
+
+
+def cpu_baseline(name: str, tokens: int):
+    from kv_cache_compression_03_gb300 import synthetic
+    bits = synthetic.generate(name, num_tokens=tokens)
+    dt, raw, nth, _ = oracle_sample(name, bits)
+    p, _, _ = workload_info(name)
+    return {"value": round(raw / dt / 1e9, 4), "unit": "GB/s", "cores": nth, "kind": "oracle",
+            "sample": f"first {tokens} of {p['T']} tokens, all {p['L']} layers, K and V "
+                      f"({raw / 1e6:.1f} MB raw bf16), encode+decode, {dt:.2f} s wall"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    from kv_cache_compression_03_gb300 import synthetic
+    p, _, _ = workload_info(args.workload)
+    tokens = args.cpu_tokens
+    bits = synthetic.generate(args.workload, num_tokens=tokens)
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, bits)
+    times = []
+    raw = 0
+    nth = 1
+    for _ in range(args.steps):
+        dt, raw, nth, _ = oracle_sample(args.workload, bits)
+        times.append(dt)
+    tot = sum(times)
+    value = raw * len(times) / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot / len(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": p["L"], "tokens": p["T"],
+                   "kv_heads": p["H"], "head_size": p["D"], "chunk_tokens": p["chunk_tokens"][0],
+                   "sample_tokens": tokens},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nth,
+                         "kind": "oracle",
+                         "sample": f"first {tokens} of {p['T']} tokens per step, encode+decode"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU
+
+def run_codec(args):
+    import numpy as np
+    import torch
+
+    from kv_cache_compression_03_gb300 import cachegen as cg
+    from kv_cache_compression_03_gb300 import synthetic
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    name = args.workload
+    p, k, v = workload_info(name)
+    L, T, H, D = p["L"], p["T"], p["H"], p["D"]
+    C = H * D
+    ch = p["chunk_tokens"][0]
+
+    # CPU baseline first (before any heavy GPU work; OpenMP threads only)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(name, args.cpu_tokens)
+
+    bits = synthetic.generate(name)
+    host_kv = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(L, 2, T, H, D)
+    kv = host_kv.to(dev)
+    codec = cg.Codec(L, T, H, D, ch, k, v, device=dev)
+    sizes = codec.sizes
+    raw = sizes.raw_bytes
+    enc = codec.alloc_encoded()
+    out = torch.empty_like(kv)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        cg.cg_encode(codec.plan, kv, codec.workspace, enc.bytestream, enc.lengths, enc.cdf,
+                     enc.amax, stream)
+        cg.cg_decode(codec.plan, enc.bytestream, enc.lengths, enc.cdf, enc.amax,
+                     enc.stream_bytes, codec.workspace, out, stream)
+
+    # one checked encode to learn the stream size
+    codec.encode(kv, enc)
+    st, total = cg.cg_last_device_error(codec.plan, codec.workspace)
+    assert st == cg.CG_OK, st
+    enc.stream_bytes = total
+    container = cg.cg_container_size(codec.plan, total)
+    for _ in range(max(args.warmup, 1)):
+        step()
+    st, _ = cg.cg_last_device_error(codec.plan, codec.workspace)
+    assert st == cg.CG_OK, st
+    torch.cuda.synchronize(dev)
+
+    launches_per_step = sizes.encode_launches + sizes.decode_launches
+    cg.cg_profile_enable(codec.plan, launches_per_step * args.steps + 8)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_local = e0.elapsed_time(e1)
+    prof = cg.cg_profile_read(codec.plan)
+    cg.cg_profile_enable(codec.plan, 0)
+    st, _ = cg.cg_last_device_error(codec.plan, codec.workspace)
+    assert st == cg.CG_OK, st
+    ms_total = aggregate_max(ms_local, world, dev)
+    ms_step = ms_total / args.steps
+    value = world * raw * args.steps / (ms_total * 1e-3) / 1e9
+
+    enc_names = ("k_encode_tiles", "k_scan_tiles(encode)", "k_pack")
+    dec_names = ("k_tile_sums", "k_scan_tiles(decode)", "k_decode_tiles")
+    t_enc = sum(prof[n][1] for n in enc_names if n in prof) / args.steps
+    t_dec = sum(prof[n][1] for n in dec_names if n in prof) / args.steps
+
+    # dominant kernel and its roofline
+    top = max(prof.items(), key=lambda kv_: kv_[1][1])
+    kname, (klaunch, kms) = top
+    side_bytes = 4 * sizes.num_scales + 4 * sizes.num_streams + 2 * sizes.cdf_entries
+    alg_bytes = raw + side_bytes + total     # read raw, write all sections (or the reverse)
+    per_launch_ms = kms / klaunch
+    achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    traffic = recorded_traffic(kname, name)
+    roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": int(alg_bytes),
+            "ms_per_launch": round(per_launch_ms, 4)}
+
+    # end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = torch.empty_like(host_kv, device="cpu").pin_memory()
+        host_in.copy_(host_kv)
+        host_out = torch.empty_like(host_in).pin_memory()
+        host_blob = torch.empty(container, dtype=torch.uint8).pin_memory()
+        kv_dev = torch.empty_like(kv)
+        enc2 = codec.alloc_encoded()
+        n_e2e = max(2, min(args.steps, 5))
+
+        def e2e_step():
+            kv_dev.copy_(host_in, non_blocking=True)
+            cg.cg_encode(codec.plan, kv_dev, codec.workspace, enc.bytestream, enc.lengths,
+                         enc.cdf, enc.amax, stream)
+            st_, sb = cg.cg_last_device_error(codec.plan, codec.workspace, stream)
+            n = cg.cg_serialize(codec.plan, enc.bytestream, enc.lengths, enc.cdf, enc.amax, sb,
+                                host_blob, stream)
+            cg.cg_deserialize(codec.plan, host_blob[:n], enc2.bytestream, enc2.lengths,
+                              enc2.cdf, enc2.amax, stream)
+            cg.cg_decode(codec.plan, enc2.bytestream, enc2.lengths, enc2.cdf, enc2.amax, sb,
+                         codec.workspace, out, stream)
+            host_out.copy_(out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            return st_, n
+
+        e2e_step()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            st_, n = e2e_step()
+        t_e2e = aggregate_max(time.perf_counter() - t0, world, dev)
+        assert st_ == cg.CG_OK
+        assert torch.equal(host_out.view(torch.int16), out.view(torch.int16).cpu())
+        e2e = {"value": round(world * raw * n_e2e / t_e2e / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(raw + n), "d2h_bytes_per_step": int(n + raw),
+               "steps": n_e2e, "path": "pinned host kv -> H2D -> cg_encode -> cg_serialize "
+               "(D2H container) -> cg_deserialize (H2D) -> cg_decode -> D2H kv"}
+
+    if rank != 0:
+        return 0
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": name, "layers": L, "tokens": T, "kv_heads": H, "head_size": D,
+                   "chunk_tokens": ch, "group_tokens": 256,
+                   "bins": {"k": [list(s) for s in k], "v": [list(s) for s in v]},
+                   "l2": "inputs larger than L2 (raw KV per step %.2f GB)" % (raw / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "encode_gbs": round(raw / (t_enc * 1e-3) / 1e9, 2),
+        "decode_gbs": round(raw / (t_dec * 1e-3) / 1e9, 2),
+        "encode_hbm_frac": round((raw + side_bytes + total) / (t_enc * 1e-3) / 1e9 / peak, 4),
+        "decode_hbm_frac": round((raw + side_bytes + total) / (t_dec * 1e-3) / 1e9 / peak, 4),
+        "compression_ratio": round(raw / container, 4),
+        "stream_bits_per_value": round(8 * total / (raw / 2), 4),
+        "container_bytes": int(container),
+        "kernels": {n: {"launches": c, "ms_per_launch": round(ms / c, 4)}
+                    for n, (c, ms) in prof.items()},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": int(launches_per_step * args.steps),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["cachegen", "reference"], default="cachegen")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-tokens", type=int, default=2048,
+                    help="tokens of the workload in the CPU oracle's bounded sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_codec(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

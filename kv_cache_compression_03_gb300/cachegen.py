@@ -1,0 +1,354 @@
+"""Python binding of the CacheGen codec's C ABI (include/cachegen.h).
+
+The functions named ``cg_*`` mirror the C entry points one to one and only
+marshal arguments: every step of encoding and decoding runs in the CUDA
+kernels of ``libcachegen.so``. Device buffers are torch tensors (torch is
+used for device memory and streams only). There is no CPU fallback: if the
+library is missing or no GPU is present, the calls raise.
+
+``Codec`` wraps a plan with its buffers for the common case; ``preset_specs``
+gives the per-layer bin counts of the LMCache presets ("LMCache 中的 KV Cache
+压缩：CacheGen 编解码原理、配置方式与源码解析", §1: the first 10 K layers and the
+first 2 V layers use 32 bins, the rest 16; fewer than 10 layers: all 32).
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+import threading
+from dataclasses import dataclass
+
+CG_OK, CG_ERR_INVALID_ARG, CG_ERR_SPEC, CG_ERR_CAPACITY = 0, 1, 2, 3
+CG_ERR_NONFINITE, CG_ERR_CORRUPT, CG_ERR_TIMEOUT, CG_ERR_CUDA, CG_ERR_UNSUPPORTED = 4, 5, 6, 7, 8
+
+
+class cg_quant_spec(ct.Structure):
+    _fields_ = [("start_layer", ct.c_int32), ("end_layer", ct.c_int32), ("bins", ct.c_int32)]
+
+
+class cg_config(ct.Structure):
+    _fields_ = [("num_layers", ct.c_int32), ("num_tokens", ct.c_int32),
+                ("num_heads", ct.c_int32), ("head_size", ct.c_int32),
+                ("chunk_tokens", ct.c_int32),
+                ("kspecs", ct.POINTER(cg_quant_spec)), ("n_kspecs", ct.c_int32),
+                ("vspecs", ct.POINTER(cg_quant_spec)), ("n_vspecs", ct.c_int32)]
+
+
+class cg_sizes(ct.Structure):
+    _fields_ = [("workspace_bytes", ct.c_size_t), ("max_stream_bytes", ct.c_size_t),
+                ("cdf_entries", ct.c_size_t), ("num_streams", ct.c_size_t),
+                ("num_scales", ct.c_size_t), ("raw_bytes", ct.c_size_t),
+                ("num_groups", ct.c_int32), ("num_tiles", ct.c_int32),
+                ("encode_launches", ct.c_int32), ("decode_launches", ct.c_int32)]
+
+
+class cg_encoded(ct.Structure):
+    _fields_ = [("bytestream", ct.c_void_p), ("bytestream_capacity", ct.c_size_t),
+                ("lengths", ct.c_void_p), ("cdf", ct.c_void_p), ("amax", ct.c_void_p)]
+
+
+class cg_kernel_profile(ct.Structure):
+    _fields_ = [("kernel", ct.c_char_p), ("launches", ct.c_int64), ("total_ms", ct.c_double)]
+
+
+class CacheGenError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {cg_status_string(status)} ({status})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libcachegen.so")
+
+
+def load(build_if_missing: bool = True) -> ct.CDLL:
+    """Load libcachegen.so (building it with nvcc when absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if build_if_missing:
+            from . import build as _build
+            path = _build.build()
+        if not os.path.exists(path):
+            raise ImportError(f"libcachegen.so not found at {path}; run build() first")
+        L = ct.CDLL(path)
+        P, sz, u64 = ct.c_void_p, ct.c_size_t, ct.c_uint64
+        st = ct.c_int
+        sigs = {
+            "cg_plan_create": (st, [ct.POINTER(cg_config), ct.POINTER(ct.c_void_p)]),
+            "cg_plan_destroy": (None, [P]),
+            "cg_plan_sizes": (st, [P, ct.POINTER(cg_sizes)]),
+            "cg_encode": (st, [P, P, P, sz, ct.POINTER(cg_encoded), P]),
+            "cg_decode": (st, [P, ct.POINTER(cg_encoded), u64, P, sz, P, P]),
+            "cg_last_device_error": (st, [P, P, ct.POINTER(ct.c_int), ct.POINTER(u64), P]),
+            "cg_container_size": (st, [P, u64, ct.POINTER(sz)]),
+            "cg_serialize": (st, [P, ct.POINTER(cg_encoded), u64, P, sz, ct.POINTER(sz), P]),
+            "cg_container_open": (st, [P, sz, ct.POINTER(ct.c_void_p), ct.POINTER(u64)]),
+            "cg_deserialize": (st, [P, P, sz, ct.POINTER(cg_encoded), P]),
+            "cg_status_string": (ct.c_char_p, [st]),
+            "cg_profile_enable": (st, [P, ct.c_int32]),
+            "cg_profile_read": (st, [P, ct.POINTER(cg_kernel_profile), ct.c_int32,
+                                     ct.POINTER(ct.c_int32)]),
+        }
+        for name, (res, args) in sigs.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+        return L
+
+
+def _check(st: int, what: str):
+    if st != CG_OK:
+        raise CacheGenError(st, what)
+
+
+def _stream_handle(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ct.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> int:
+    return t.data_ptr() if t is not None else 0
+
+
+# ------------------------------------------------------------ C ABI mirror
+
+def cg_status_string(status: int) -> str:
+    try:
+        return load(build_if_missing=False).cg_status_string(status).decode()
+    except Exception:  # library not loadable: still give a message
+        return f"status {status}"
+
+
+def _specs_array(specs):
+    arr = (cg_quant_spec * len(specs))()
+    for i, (s, e, b) in enumerate(specs):
+        arr[i] = cg_quant_spec(int(s), int(e), int(b))
+    return arr
+
+
+def cg_plan_create(num_layers, num_tokens, num_heads, head_size, chunk_tokens, kspecs, vspecs):
+    """Validate a configuration and return an opaque plan handle (int)."""
+    ka, va = _specs_array(kspecs), _specs_array(vspecs)
+    cfg = cg_config(num_layers, num_tokens, num_heads, head_size, chunk_tokens,
+                    ka, len(kspecs), va, len(vspecs))
+    h = ct.c_void_p()
+    _check(load().cg_plan_create(ct.byref(cfg), ct.byref(h)), "cg_plan_create")
+    return h.value
+
+
+def cg_plan_destroy(plan) -> None:
+    if plan:
+        load().cg_plan_destroy(ct.c_void_p(plan))
+
+
+def cg_plan_sizes(plan) -> cg_sizes:
+    s = cg_sizes()
+    _check(load().cg_plan_sizes(ct.c_void_p(plan), ct.byref(s)), "cg_plan_sizes")
+    return s
+
+
+def _encoded_struct(bytestream, lengths, cdf, amax) -> cg_encoded:
+    return cg_encoded(_ptr(bytestream), bytestream.numel() * bytestream.element_size(),
+                      _ptr(lengths), _ptr(cdf), _ptr(amax))
+
+
+def cg_encode(plan, kv, workspace, bytestream, lengths, cdf, amax, stream=None) -> None:
+    enc = _encoded_struct(bytestream, lengths, cdf, amax)
+    _check(load().cg_encode(ct.c_void_p(plan), ct.c_void_p(_ptr(kv)), ct.c_void_p(_ptr(workspace)),
+                            workspace.numel(), ct.byref(enc), _stream_handle(stream)), "cg_encode")
+
+
+def cg_decode(plan, bytestream, lengths, cdf, amax, stream_bytes, workspace, kv_out,
+              stream=None) -> None:
+    enc = _encoded_struct(bytestream, lengths, cdf, amax)
+    _check(load().cg_decode(ct.c_void_p(plan), ct.byref(enc), int(stream_bytes),
+                            ct.c_void_p(_ptr(workspace)), workspace.numel(),
+                            ct.c_void_p(_ptr(kv_out)), _stream_handle(stream)), "cg_decode")
+
+
+def cg_last_device_error(plan, workspace, stream=None):
+    """Wait for the stream; return (device status, total stream bytes)."""
+    st = ct.c_int(0)
+    tot = ct.c_uint64(0)
+    _check(load().cg_last_device_error(ct.c_void_p(plan), ct.c_void_p(_ptr(workspace)),
+                                       ct.byref(st), ct.byref(tot), _stream_handle(stream)),
+           "cg_last_device_error")
+    return st.value, tot.value
+
+
+def cg_container_size(plan, stream_bytes) -> int:
+    n = ct.c_size_t(0)
+    _check(load().cg_container_size(ct.c_void_p(plan), int(stream_bytes), ct.byref(n)),
+           "cg_container_size")
+    return n.value
+
+
+def cg_serialize(plan, bytestream, lengths, cdf, amax, stream_bytes, host_out, stream=None) -> int:
+    """Write the container into host_out (a uint8 CPU tensor, ideally
+    pinned); returns the bytes written."""
+    enc = _encoded_struct(bytestream, lengths, cdf, amax)
+    n = ct.c_size_t(0)
+    _check(load().cg_serialize(ct.c_void_p(plan), ct.byref(enc), int(stream_bytes),
+                               ct.c_void_p(host_out.data_ptr()), host_out.numel(), ct.byref(n),
+                               _stream_handle(stream)), "cg_serialize")
+    return n.value
+
+
+def cg_container_open(host_in):
+    """Parse a container header (uint8 CPU tensor); return (plan, stream_bytes)."""
+    h = ct.c_void_p()
+    sb = ct.c_uint64(0)
+    _check(load().cg_container_open(ct.c_void_p(host_in.data_ptr()), host_in.numel(),
+                                    ct.byref(h), ct.byref(sb)), "cg_container_open")
+    return h.value, sb.value
+
+
+def cg_deserialize(plan, host_in, bytestream, lengths, cdf, amax, stream=None) -> None:
+    enc = _encoded_struct(bytestream, lengths, cdf, amax)
+    _check(load().cg_deserialize(ct.c_void_p(plan), ct.c_void_p(host_in.data_ptr()),
+                                 host_in.numel(), ct.byref(enc), _stream_handle(stream)),
+           "cg_deserialize")
+
+
+def cg_profile_enable(plan, max_launches: int) -> None:
+    _check(load().cg_profile_enable(ct.c_void_p(plan), int(max_launches)), "cg_profile_enable")
+
+
+def cg_profile_read(plan) -> dict:
+    """{kernel name: (launches, total ms)} since the last read."""
+    arr = (cg_kernel_profile * 16)()
+    n = ct.c_int32(0)
+    _check(load().cg_profile_read(ct.c_void_p(plan), arr, 16, ct.byref(n)), "cg_profile_read")
+    return {arr[i].kernel.decode(): (int(arr[i].launches), float(arr[i].total_ms))
+            for i in range(min(n.value, 16))}
+
+
+# ------------------------------------------------------------- convenience
+
+def preset_specs(num_layers: int):
+    """(kspecs, vspecs) of the LMCache presets for a model with num_layers
+    layers: K's first 10 and V's first 2 layers at 32 bins, the rest at 16;
+    with fewer than 10 layers every layer uses 32 bins."""
+    L = int(num_layers)
+    if L <= 0:
+        raise ValueError("num_layers must be positive")
+    if L < 10:
+        return [(0, L, 32)], [(0, L, 32)]
+    k = [(0, 10, 32)] + ([(10, L, 16)] if L > 10 else [])
+    v = [(0, 2, 32), (2, L, 16)]
+    return k, v
+
+
+@dataclass
+class Encoded:
+    """Device buffers of one encoded KV blob."""
+    bytestream: "object"   # uint8 [capacity]
+    lengths: "object"      # int32 [2*L*T]
+    cdf: "object"          # uint16 (stored as int16) [cdf_entries]
+    amax: "object"         # float32 [2, L, T]
+    stream_bytes: int
+
+    def nbytes(self) -> int:
+        return int(self.stream_bytes) + self.lengths.numel() * 4 + self.cdf.numel() * 2 + \
+            self.amax.numel() * 4
+
+
+class Codec:
+    """A plan plus its device buffers, for encoding/decoding one shape."""
+
+    def __init__(self, num_layers, num_tokens, num_heads, head_size, chunk_tokens=256,
+                 kspecs=None, vspecs=None, device="cuda"):
+        import torch
+        if kspecs is None or vspecs is None:
+            k, v = preset_specs(num_layers)
+            kspecs = kspecs or k
+            vspecs = vspecs or v
+        self.L, self.T, self.H, self.D = num_layers, num_tokens, num_heads, head_size
+        self.chunk_tokens = chunk_tokens
+        self.kspecs, self.vspecs = list(kspecs), list(vspecs)
+        self.plan = cg_plan_create(num_layers, num_tokens, num_heads, head_size, chunk_tokens,
+                                   self.kspecs, self.vspecs)
+        self.sizes = cg_plan_sizes(self.plan)
+        self.device = torch.device(device)
+        self.workspace = torch.empty(self.sizes.workspace_bytes, dtype=torch.uint8,
+                                     device=self.device)
+
+    def __del__(self):
+        try:
+            cg_plan_destroy(self.plan)
+        except Exception:
+            pass
+
+    def alloc_encoded(self, capacity=None) -> Encoded:
+        import torch
+        cap = int(capacity or self.sizes.max_stream_bytes)
+        cap = (cap + 15) // 16 * 16
+        d = self.device
+        return Encoded(torch.empty(cap, dtype=torch.uint8, device=d),
+                       torch.empty(self.sizes.num_streams, dtype=torch.int32, device=d),
+                       torch.empty(self.sizes.cdf_entries, dtype=torch.int16, device=d),
+                       torch.empty((2, self.L, self.T), dtype=torch.float32, device=d), 0)
+
+    def encode(self, kv, out: Encoded | None = None, sync: bool = True, stream=None) -> Encoded:
+        """kv: bf16 cuda tensor [L, 2, T, H, D] (contiguous)."""
+        import torch
+        assert kv.dtype == torch.bfloat16 and kv.is_cuda and kv.is_contiguous()
+        assert kv.numel() == self.sizes.raw_bytes // 2
+        out = out or self.alloc_encoded()
+        cg_encode(self.plan, kv, self.workspace, out.bytestream, out.lengths, out.cdf, out.amax,
+                  stream)
+        if sync:
+            st, total = cg_last_device_error(self.plan, self.workspace, stream)
+            _check(st, "cg_encode (device)")
+            out.stream_bytes = total
+        return out
+
+    def decode(self, enc: Encoded, kv_out=None, sync: bool = True, stream=None):
+        import torch
+        if kv_out is None:
+            kv_out = torch.empty((self.L, 2, self.T, self.H, self.D), dtype=torch.bfloat16,
+                                 device=self.device)
+        cg_decode(self.plan, enc.bytestream, enc.lengths, enc.cdf, enc.amax, enc.stream_bytes,
+                  self.workspace, kv_out, stream)
+        if sync:
+            st, _ = cg_last_device_error(self.plan, self.workspace, stream)
+            _check(st, "cg_decode (device)")
+        return kv_out
+
+    def to_bytes(self, enc: Encoded, host_out=None, stream=None):
+        """Serialise to a uint8 CPU tensor (pinned unless host_out is given)."""
+        import torch
+        n = cg_container_size(self.plan, enc.stream_bytes)
+        if host_out is None:
+            host_out = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        w = cg_serialize(self.plan, enc.bytestream, enc.lengths, enc.cdf, enc.amax,
+                         enc.stream_bytes, host_out, stream)
+        return host_out[:w]
+
+    @staticmethod
+    def from_bytes(host_in, device="cuda", stream=None):
+        """Open a container (uint8 CPU tensor); return (codec, encoded)."""
+        plan, sb = cg_container_open(host_in)
+        try:
+            import struct
+            hdr = bytes(host_in[:48].numpy())
+            L, T, H, D, ch, nk, nv = struct.unpack_from("<7i", hdr, 8)
+            raw = bytes(host_in[48:48 + 12 * (nk + nv)].numpy())
+            specs = [struct.unpack_from("<3i", raw, 12 * i) for i in range(nk + nv)]
+        finally:
+            cg_plan_destroy(plan)
+        codec = Codec(L, T, H, D, ch, specs[:nk], specs[nk:], device=device)
+        enc = codec.alloc_encoded(capacity=max(16, sb))
+        enc.stream_bytes = sb
+        cg_deserialize(codec.plan, host_in, enc.bytestream, enc.lengths, enc.cdf, enc.amax,
+                       stream)
+        return codec, enc

@@ -1,0 +1,82 @@
+// Internal declarations shared by the codec's host API and its kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "cachegen.h"
+
+// Limits of this build.
+#define CG_MAX_LAYERS 256
+#define CG_MAX_CHANNELS 4096
+// Tokens per group: the encoder works in batches of at most 256 tokens,
+// each with its own CDFs ("LMCache 中的 KV Cache 压缩：CacheGen 编解码原理、配置方式与
+// 源码解析", §4).
+#define CG_GROUP_TOKENS 256
+// Threads per tile CTA: one per token of a group.
+#define CG_TILE_THREADS 256
+// Shared memory a CTA may use on sm_103a.
+#define CG_SMEM_LIMIT (227 * 1024)
+
+// Workspace status block (first 256 bytes of every workspace).
+#define CG_WS_STATUS_BYTES 256
+#define CG_WS_STATUS 0        // u32 first device error (cg_status), 0 = none
+#define CG_WS_TOTAL 8         // u64 total stream bytes
+
+// Per-launch description of the tiles. A tile is one (group, K/V, layer);
+// tile index = (group * 2 + kv) * L + layer, which is also the order of
+// the tiles' streams, CDF blocks and bytes.
+struct cg_tile_params {
+    int32_t L, T, C, chunk_tokens;
+    int32_t ngroups, ntiles;
+    int32_t groups_per_object, full_objects;
+    uint64_t cdf_per_group;  // CDF entries of one group (all K/V, layers)
+    uint32_t slot_stride;    // bytes of one stream slot in the workspace
+    uint32_t pad_;
+    uint8_t bins[2][CG_MAX_LAYERS];
+    uint32_t cdf_off[2][CG_MAX_LAYERS];  // offset of (kv, l) inside a group block
+};
+
+// Kernel identities for per-kernel timing.
+enum cg_kernel_id {
+    CG_K_ENCODE_TILES = 0,
+    CG_K_SCAN_ENCODE,
+    CG_K_PACK,
+    CG_K_TILE_SUMS,
+    CG_K_SCAN_DECODE,
+    CG_K_DECODE_TILES,
+    CG_K_COUNT
+};
+
+struct cg_profiler {
+    std::vector<cudaEvent_t> events;  // 2 per recorded launch
+    std::vector<int8_t> ids;
+    int32_t used = 0;
+    // bracket one launch; both are no-ops when profiling is off or full
+    void begin(int id, cudaStream_t s);
+    void end(cudaStream_t s);
+};
+
+struct cg_plan {
+    int32_t L, T, H, D, C, chunk_tokens;
+    std::vector<cg_quant_spec> kspecs, vspecs;
+    cg_tile_params tp;
+    int32_t max_bins;
+    uint64_t num_streams;
+    uint64_t cdf_entries;
+    // workspace layout (byte offsets)
+    size_t ws_tile_totals, ws_tile_base, ws_symbols, ws_slots, ws_bytes;
+    size_t max_stream_bytes;
+    size_t smem_encode, smem_decode;
+    mutable cg_profiler prof;
+};
+
+cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const cg_encoded *out,
+                             cudaStream_t stream);
+cudaError_t cg_launch_decode(const cg_plan *p, const cg_encoded *in, uint64_t stream_bytes,
+                             void *ws, void *kv_out, cudaStream_t stream);
+const char *cg_kernel_name(int id);
+int cg_encode_launch_count();
+int cg_decode_launch_count();

@@ -1,0 +1,157 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+exports every function include/cachegen.h declares, configuration
+validation matches the oracle's, sizes follow the layout, and a container
+written by the oracle opens with the same plan."""
+import ctypes as ct
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from kv_cache_compression_03_gb300 import cachegen as cg
+from kv_cache_compression_03_gb300 import synthetic
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cachegen.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(cg_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return cg.load()
+
+
+def test_header_declares_boundary():
+    names = _declared()
+    for want in ("cg_plan_create", "cg_plan_destroy", "cg_plan_sizes", "cg_encode", "cg_decode",
+                 "cg_last_device_error", "cg_container_size", "cg_serialize",
+                 "cg_container_open", "cg_deserialize", "cg_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    path = cg.library_path()
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    for name in _declared():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_header_compiles_as_c():
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c",
+                        HEADER], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def _plan(L=32, T=1024, H=8, D=128, ch=256, k=None, v=None):
+    if k is None:
+        k, v = cg.preset_specs(L)
+    return cg.cg_plan_create(L, T, H, D, ch, k, v)
+
+
+def test_plan_sizes_match_layout(orc):
+    for name in synthetic.WORKLOADS:
+        p = synthetic.WORKLOADS[name]
+        k, v = synthetic.workload_specs(name)
+        for ch in p["chunk_tokens"]:
+            plan = cg.cg_plan_create(p["L"], p["T"], p["H"], p["D"], ch, k, v)
+            try:
+                s = cg.cg_plan_sizes(plan)
+                C = p["H"] * p["D"]
+                assert s.num_streams == 2 * p["L"] * p["T"] == s.num_scales
+                assert s.raw_bytes == 2 * p["L"] * p["T"] * C * 2
+                assert s.num_groups == len(orc.groups(p["T"], ch)[0])
+                assert s.num_tiles == s.num_groups * 2 * p["L"]
+                assert s.cdf_entries == orc.cdf_entries(p["L"], p["T"], C, ch, k, v)
+                assert s.max_stream_bytes >= s.num_streams * (C + 1)
+                assert s.encode_launches >= 1 and s.decode_launches >= 1
+                assert s.workspace_bytes > 0
+            finally:
+                cg.cg_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("k,v", [
+    ([(0, 10, 32), (9, 32, 16)], [(0, 32, 16)]),
+    ([(0, 32, 16)], [(0, 2, 32), (3, 32, 16)]),
+    ([(0, 32, 15)], [(0, 32, 16)]),
+    ([(0, 32, 2)], [(0, 32, 16)]),
+    ([(0, 32, 66)], [(0, 32, 16)]),
+    ([(0, 33, 16)], [(0, 32, 16)]),
+])
+def test_plan_rejects_bad_specs(orc, k, v):
+    with pytest.raises(cg.CacheGenError) as e:
+        _plan(k=k, v=v)
+    assert e.value.status == cg.CG_ERR_SPEC
+    # the oracle rejects the same lists
+    with pytest.raises(orc.OracleError):
+        orc.layer_bins(32, k)
+        orc.layer_bins(32, v)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 1024, 8, 128, 256), cg.CG_ERR_INVALID_ARG),
+    ((32, 0, 8, 128, 256), cg.CG_ERR_INVALID_ARG),
+    ((32, 1024, 8, 128, 0), cg.CG_ERR_INVALID_ARG),
+    ((32, 1024, 1, 12, 256), cg.CG_ERR_INVALID_ARG),     # C not a multiple of 8
+    ((32, 1024, 64, 128, 256), cg.CG_ERR_UNSUPPORTED),   # C = 8192 > 4096
+    ((300, 16, 8, 128, 256), cg.CG_ERR_UNSUPPORTED),     # more than 256 layers
+])
+def test_plan_rejects_bad_shapes(args, code):
+    L = args[0]
+    k, v = cg.preset_specs(max(L, 1))
+    with pytest.raises(cg.CacheGenError) as e:
+        cg.cg_plan_create(*args, k, v)
+    assert e.value.status == code
+
+
+def test_preset_specs():
+    assert cg.preset_specs(32) == ([(0, 10, 32), (10, 32, 16)], [(0, 2, 32), (2, 32, 16)])
+    assert cg.preset_specs(40) == ([(0, 10, 32), (10, 40, 16)], [(0, 2, 32), (2, 40, 16)])
+    assert cg.preset_specs(6) == ([(0, 6, 32)], [(0, 6, 32)])
+    assert cg.preset_specs(10) == ([(0, 10, 32)], [(0, 2, 32), (2, 10, 16)])
+    for L in (12, 32, 40):
+        assert cg.preset_specs(L) == synthetic.workload_specs(
+            {12: "opt125m_t256", 32: "mistral7b_t1k", 40: "glm4_9b_t32k"}[L])
+
+
+def test_container_open_reads_oracle_container(orc):
+    import torch
+    name = "opt125m_t256"
+    kv = synthetic.generate(name, num_tokens=300)
+    L, _, T, C = kv.shape
+    k, v = synthetic.workload_specs(name)
+    enc = orc.encode(kv, 256, k, v)
+    blob = orc.serialize(enc, L, T, 12, 64, 256, k, v)
+    host = torch.from_numpy(np.frombuffer(blob, dtype=np.uint8).copy())
+    plan, sb = cg.cg_container_open(host)
+    try:
+        assert sb == enc["stream_bytes"]
+        assert cg.cg_container_size(plan, sb) == len(blob)
+        s = cg.cg_plan_sizes(plan)
+        assert s.cdf_entries == enc["cdf"].size and s.num_streams == 2 * L * T
+    finally:
+        cg.cg_plan_destroy(plan)
+    # a damaged header is rejected
+    bad = host.clone()
+    bad[0] = 0
+    with pytest.raises(cg.CacheGenError) as e:
+        cg.cg_container_open(bad)
+    assert e.value.status == cg.CG_ERR_CORRUPT
+    short = host[:-1].clone()
+    with pytest.raises(cg.CacheGenError) as e:
+        cg.cg_container_open(short)
+    assert e.value.status == cg.CG_ERR_CORRUPT
+
+
+def test_status_strings(lib):
+    assert cg.cg_status_string(0) == "ok"
+    assert "capacity" in cg.cg_status_string(cg.CG_ERR_CAPACITY)
