@@ -104,6 +104,7 @@ def test_plan_rejects_bad_specs(orc, k, v):
     ((32, 1024, 1, 12, 256), cg.CG_ERR_INVALID_ARG),     # C not a multiple of 8
     ((32, 1024, 64, 128, 256), cg.CG_ERR_UNSUPPORTED),   # C = 8192 > 4096
     ((300, 16, 8, 128, 256), cg.CG_ERR_UNSUPPORTED),     # more than 256 layers
+    ((2, 16, 32, 128, 256), cg.CG_ERR_UNSUPPORTED),      # C = 4096 at 32 bins: CDF table too big
 ])
 def test_plan_rejects_bad_shapes(args, code):
     L = args[0]

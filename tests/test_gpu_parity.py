@@ -106,7 +106,8 @@ EDGE = [
     (2, 300, 2, 32, 256, [(0, 2, 32)], [(0, 2, 16)], "constant"),   # one value per row
     (2, 300, 2, 32, 256, [(0, 2, 32)], [(0, 2, 16)], "extreme"),    # huge and tiny values
     (1, 513, 8, 64, 1000, [(0, 1, 64)], [(0, 1, 4)], "normal"),     # chunk > T
-    (2, 64, 8, 512, 64, [(0, 2, 32)], [(0, 2, 16)], "normal"),      # C = 4096
+    (2, 64, 8, 512, 64, [(0, 2, 16)], [(0, 2, 16)], "normal"),      # C = 4096 (16 bins)
+    (2, 100, 16, 128, 64, [(0, 2, 32)], [(0, 1, 16), (1, 2, 32)], "normal"),  # C = 2048
 ]
 
 
