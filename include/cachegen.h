@@ -199,6 +199,31 @@ cg_status cg_container_open(const void *host_in, size_t len, cg_plan **plan_out,
 cg_status cg_deserialize(const cg_plan *plan, const void *host_in, size_t len,
                          const cg_encoded *dev_out, cg_stream_t stream);
 
+/* Bytes of the fixed scratch array that cg_encode_noalloc uses (64 MiB). */
+#define CG_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* Encode like cg_encode, but without a workspace argument and without any
+ * device allocation: for callers that cannot allocate device memory when
+ * they encode, such as a serving engine that has already reserved nearly
+ * all of the GPU for its KV cache pool, or a latency-critical path where
+ * cudaMalloc/cudaFree (which may synchronise the device) is not allowed.
+ * The pages describe no such call; it is an addition of this library.
+ * The scratch is one array of CG_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library, which every GPU that loads the library keeps until the process
+ * exits. A plan whose workspace_bytes exceed it is rejected with
+ * CG_ERR_UNSUPPORTED before anything is enqueued. The caller still passes
+ * kv and the output buffers (same rules as cg_encode) and status_out, a
+ * device buffer of at least 16 bytes that receives the device status word
+ * and the total stream bytes (read it with cg_last_device_error, passing
+ * status_out as the workspace). The first call on each device looks up the
+ * array's device address (with that device current); make that first call
+ * before any stream capture. All calls share the one array and it keeps the
+ * last call's contents (each call clears what must start at zero): calls
+ * that can overlap on the GPU, from any stream or thread, race on it, so
+ * serialise them. Asynchronous on stream. */
+cg_status cg_encode_noalloc(const cg_plan *plan, const void *kv, const cg_encoded *out,
+                            void *status_out, cg_stream_t stream);
+
 /* Per-kernel timing, for profiling. When enabled, each kernel that
  * cg_encode/cg_decode enqueue is bracketed by two CUDA events on the launch
  * stream (up to max_launches kernels are recorded; later ones are not).

@@ -92,6 +92,7 @@ def load(build_if_missing: bool = True) -> ct.CDLL:
             "cg_container_open": (st, [P, sz, ct.POINTER(ct.c_void_p), ct.POINTER(u64)]),
             "cg_deserialize": (st, [P, P, sz, ct.POINTER(cg_encoded), P]),
             "cg_status_string": (ct.c_char_p, [st]),
+            "cg_encode_noalloc": (st, [P, P, ct.POINTER(cg_encoded), P, P]),
             "cg_profile_enable": (st, [P, ct.c_int32]),
             "cg_profile_read": (st, [P, ct.POINTER(cg_kernel_profile), ct.c_int32,
                                      ct.POINTER(ct.c_int32)]),
@@ -165,6 +166,18 @@ def cg_encode(plan, kv, workspace, bytestream, lengths, cdf, amax, stream=None) 
     enc = _encoded_struct(bytestream, lengths, cdf, amax)
     _check(load().cg_encode(ct.c_void_p(plan), ct.c_void_p(_ptr(kv)), ct.c_void_p(_ptr(workspace)),
                             workspace.numel(), ct.byref(enc), _stream_handle(stream)), "cg_encode")
+
+
+def cg_encode_noalloc(plan, kv, bytestream, lengths, cdf, amax, status_out, stream=None) -> None:
+    """cg_encode with the library's fixed scratch array instead of a
+    workspace, for callers that cannot allocate device memory at encode time
+    (see include/cachegen.h). status_out: a device tensor of >= 16 bytes that
+    receives the status word and total stream bytes; read it with
+    cg_last_device_error(plan, status_out)."""
+    enc = _encoded_struct(bytestream, lengths, cdf, amax)
+    _check(load().cg_encode_noalloc(ct.c_void_p(plan), ct.c_void_p(_ptr(kv)), ct.byref(enc),
+                                    ct.c_void_p(_ptr(status_out)), _stream_handle(stream)),
+           "cg_encode_noalloc")
 
 
 def cg_decode(plan, bytestream, lengths, cdf, amax, stream_bytes, workspace, kv_out,
