@@ -170,13 +170,33 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
     tp.slot_stride = (uint32_t)align_up((size_t)C + 16, 16);
     p->max_stream_bytes = align_up((size_t)p->num_streams * (C + 2), 16);
 
-    // shared memory: CDF table [C][maxb+1] u16 (+ per-token factors)
-    const size_t table = align_up((size_t)C * (maxb + 1) * 2, 16);
-    p->smem_encode = table + CG_GROUP_TOKENS * sizeof(float);
-    p->smem_decode = table;
-    if (p->smem_encode > CG_SMEM_LIMIT - 2048) {
-        delete p;
-        return CG_ERR_UNSUPPORTED;
+    // launch classes: (kv, layer) pairs grouped by bin count
+    {
+        int32_t k = 0;
+        for (int32_t b = 4; b <= 64; b += 2) {
+            cg_bin_class cl;
+            cl.begin = k;
+            cl.bins = b;
+            for (int kv = 0; kv < 2; ++kv)
+                for (int32_t l = 0; l < L; ++l)
+                    if (tp.bins[kv][l] == b)
+                        tp.order[k++] = (uint16_t)((kv << 8) | l);
+            cl.count = k - cl.begin;
+            if (cl.count == 0)
+                continue;
+            cl.smem_encode = cg_smem_encode(C, b);
+            // the decoder's bucket table takes what shared memory is left
+            cl.bucket_log2 = 5;
+            while (cl.bucket_log2 > 0 &&
+                   cg_smem_decode(C, b, cl.bucket_log2) > CG_SMEM_LIMIT - 2048)
+                --cl.bucket_log2;
+            cl.smem_decode = cg_smem_decode(C, b, cl.bucket_log2);
+            if (cl.smem_encode > CG_SMEM_LIMIT - 2048 || cl.smem_decode > CG_SMEM_LIMIT - 2048) {
+                delete p;
+                return CG_ERR_UNSUPPORTED;
+            }
+            p->classes.push_back(cl);
+        }
     }
 
     // workspace: status | tile totals | tile bases | symbols | slots
@@ -265,8 +285,8 @@ cg_status cg_plan_sizes(const cg_plan *p, cg_sizes *out)
     out->raw_bytes = (size_t)p->num_streams * p->C * 2;
     out->num_groups = p->tp.ngroups;
     out->num_tiles = p->tp.ntiles;
-    out->encode_launches = cg_encode_launch_count();
-    out->decode_launches = cg_decode_launch_count();
+    out->encode_launches = cg_encode_launch_count(p);
+    out->decode_launches = cg_decode_launch_count(p);
     return CG_OK;
 }
 

@@ -7,26 +7,26 @@
 // of Witten, Neal & Cleary, CACM 30(6), 1987.
 //
 // Work decomposition: one CTA of 256 threads per tile = (token group,
-// K/V, layer). Encode (one kernel per tile, then a tile scan and a pack):
-//   A1  warp per token row: amax over the C channels (16-byte loads, the
-//       |x| maximum taken on bf16 bit patterns), scale factor per token;
-//   A2  thread per channel pair: quantise every token of the group,
-//       histogram in shared memory (each thread owns its channels' rows,
-//       so no atomics), write the symbols to a scratch row per stream;
-//   B   thread per channel pair: integer CDF in place of the histogram,
-//       copied out as the tile's CDF block;
-//   C   thread per token: arithmetic-code the token's stream over the C
-//       channels with the shared-memory CDF rows, renormalising in bulk
-//       (leading-zero counts instead of a bit loop), into a stream slot.
-// Pack: block scan of the tile's lengths + the tile's base offset, then
-// the slots are copied to their packed position.
-// Decode: per tile, the CDF block is staged in shared memory, the lengths
-// are scanned, and each thread decodes one stream (binary search of the
-// CDF row with the coder's exact multiply-compare), dequantising into the
-// bf16 output row.
+// K/V, layer); the tiles of each bin count are one launch, with shared
+// memory sized for that bin count. Encode (then a tile scan and a pack):
+//   A  blocks of 8 token rows: warp per row computes amax over the C
+//      channels (16-byte loads; |x| maximum on bf16 bit patterns) and the
+//      row's scale factor; then thread per channel (pair) re-reads the
+//      block (L1/L2-resident), quantises, counts into its own shared-memory
+//      histogram rows (no atomics) and writes the symbols to a scratch row
+//      per stream. The next block's amax overlaps this block's counting.
+//   B  thread per channel: integer CDF in place of the histogram, copied
+//      out as the tile's CDF block.
+//   C  thread per token: arithmetic-code the token's stream over the C
+//      channels with the shared-memory CDF rows (see Enc).
+// Pack: block scan of the tile's lengths + the tile's base, then the
+// slots are copied to their packed position. Decode: per tile, the CDF
+// block and a bucket table are staged in shared memory, the lengths are
+// scanned, and each thread decodes one stream and writes the dequantised
+// bf16 row.
 //
 // No kernel waits on another block, and every loop is bounded by the
-// tile's token and channel counts.
+// tile's token and channel counts or the alphabet size.
 
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -38,7 +38,7 @@
 namespace {
 
 constexpr int NT = CG_TILE_THREADS;
-constexpr uint32_t kQuarter = 0x40000000u;
+constexpr int kRowsPerBlock = 8;  // encoder phase A block (one row per warp)
 
 __device__ __forceinline__ void set_status(uint32_t *st, uint32_t code)
 {
@@ -46,34 +46,52 @@ __device__ __forceinline__ void set_status(uint32_t *st, uint32_t code)
 }
 
 struct Tile {
+    int32_t index;  // (g * 2 + kv) * L + l
     int32_t g, kv, l, t0, n, N;
     uint64_t first_stream;  // index of the tile's first stream
     uint64_t cdf_base;      // entry offset of the tile's CDF block
 };
 
-__device__ __forceinline__ Tile tile_of(const cg_tile_params &P, int32_t tile)
+__device__ __forceinline__ Tile make_tile(const cg_tile_params &P, int32_t g, int32_t kv,
+                                          int32_t l)
 {
     Tile t;
-    t.l = tile % P.L;
-    t.kv = (tile / P.L) & 1;
-    t.g = tile / (2 * P.L);
+    t.g = g;
+    t.kv = kv;
+    t.l = l;
+    t.index = (g * 2 + kv) * P.L + l;
     // groups: objects of chunk_tokens tokens, each cut into runs of <= 256
-    int32_t nf = P.full_objects * P.groups_per_object;
-    if (t.g < nf) {
-        int32_t o = t.g / P.groups_per_object;
-        int32_t j = t.g - o * P.groups_per_object;
+    const int32_t nf = P.full_objects * P.groups_per_object;
+    if (g < nf) {
+        const int32_t o = g / P.groups_per_object;
+        const int32_t j = g - o * P.groups_per_object;
         t.t0 = o * P.chunk_tokens + j * CG_GROUP_TOKENS;
         t.n = min(CG_GROUP_TOKENS, P.chunk_tokens - j * CG_GROUP_TOKENS);
     } else {
-        int32_t j = t.g - nf;
-        int32_t base = P.full_objects * P.chunk_tokens;
+        const int32_t j = g - nf;
+        const int32_t base = P.full_objects * P.chunk_tokens;
         t.t0 = base + j * CG_GROUP_TOKENS;
         t.n = min(CG_GROUP_TOKENS, P.T - base - j * CG_GROUP_TOKENS);
     }
-    t.N = P.bins[t.kv][t.l];
-    t.first_stream = (uint64_t)2 * P.L * t.t0 + ((uint64_t)t.kv * P.L + t.l) * (uint64_t)t.n;
-    t.cdf_base = (uint64_t)t.g * P.cdf_per_group + P.cdf_off[t.kv][t.l];
+    t.N = P.bins[kv][l];
+    t.first_stream = (uint64_t)2 * P.L * t.t0 + ((uint64_t)kv * P.L + l) * (uint64_t)t.n;
+    t.cdf_base = (uint64_t)g * P.cdf_per_group + P.cdf_off[kv][l];
     return t;
+}
+
+// Tile of block b of a class launch over the pairs order[begin, begin+count).
+__device__ __forceinline__ Tile tile_of_class(const cg_tile_params &P, int32_t begin,
+                                              int32_t count, int32_t b)
+{
+    const int32_t g = b / count;
+    const uint32_t kvl = P.order[begin + (b - g * count)];
+    return make_tile(P, g, (int32_t)(kvl >> 8), (int32_t)(kvl & 0xFFu));
+}
+
+// Tile by its global index (kernels that cover every tile).
+__device__ __forceinline__ Tile tile_by_index(const cg_tile_params &P, int32_t index)
+{
+    return make_tile(P, index / (2 * P.L), (index / P.L) & 1, index % P.L);
 }
 
 // Block-wide exclusive scan of one value per thread (256 threads).
@@ -84,7 +102,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
         if (lane >= o)
             x += y;
     }
@@ -95,7 +113,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
         uint32_t w = (lane < NT / 32) ? warp_sums[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
             if (lane >= o)
                 w += y;
         }
@@ -103,7 +121,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
             warp_sums[lane] = w;  // inclusive
     }
     __syncthreads();
-    uint32_t before = (warp > 0) ? warp_sums[warp - 1] : 0u;
+    const uint32_t before = (warp > 0) ? warp_sums[warp - 1] : 0u;
     if (total)
         *total = warp_sums[NT / 32 - 1];
     return before + x - v;
@@ -111,135 +129,220 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
 
 // ------------------------------------------------------------ quantiser
 
-// q = round_half_even(fp32(fp32(x * f) + MAX)), clamped to [0, 2*MAX]
-// (the clamp never acts on finite input; it keeps table indices in range
-// when the input holds inf/NaN, which is reported separately).
-__device__ __forceinline__ uint32_t quantise(float x, float f, float fmax, int32_t two_max)
+// q = round_half_even(fp32(fp32(x * f) + MAX)). For finite rows q lies in
+// [0, 2*MAX]; rows holding inf/NaN get f = 0, and the conversion of NaN
+// gives 0, so q stays in range for them too (they are reported separately).
+__device__ __forceinline__ uint32_t quantise(float x, float f, float fmax)
 {
-    float y = __fadd_rn(__fmul_rn(x, f), fmax);
-    int32_t q = __float2int_rn(y);
-    q = max(0, min(q, two_max));
-    return (uint32_t)q;
+    return (uint32_t)__float2int_rn(__fadd_rn(__fmul_rn(x, f), fmax));
 }
 
-// ------------------------------------------------------------ bit writer
+// floor(r * c / 2^16) for r = d + 1 <= 2^32 and c <= 65536, kept mod 2^32
+// (it is 2^32 only when r = 2^32 and c = 65536; callers work mod 2^32).
+__device__ __forceinline__ uint32_t scale16(uint32_t d, uint32_t c)
+{
+    return (uint32_t)(((uint64_t)d * c + c) >> 16);
+}
 
+// ------------------------------------------------------------ encoder
+
+// Coder state in "carry" form. The textbook coder keeps a 32-bit window
+// [low, high] and defers the bits of an interval that straddles the middle
+// (pending bits). Equivalently, keep the absolute low end of the interval:
+// its leading bits are the output, the window x holds its next 32 bits,
+// and an addition that overflows x carries into the output bits already
+// produced. The renormalisation shift S (the textbook coder's number of
+// halvings) is n, the leading bits shared by x and x + range - 1, plus k,
+// the following positions where the low end has 1 and the high end 0. The
+// textbook window equals x with its top bit cleared (that bit is 1 exactly
+// while pending bits are outstanding), so the interval arithmetic and the
+// emitted bits are the same as the bit-serial coder's.
 struct Enc {
-    uint32_t low, high, pending;
-    uint32_t nb;        // valid bits in acc (< 32 between calls)
-    uint64_t acc;
+    uint32_t x;       // window of the absolute low end
+    uint32_t d;       // range - 1
+    uint32_t a0, a1;  // output bits not yet stored: the low nb bits of (a1:a0)
+    uint32_t nb;
+    uint32_t wp;      // words stored
+    uint32_t cap;     // slot capacity in words
     uint32_t *out;
-    uint32_t nwords, cap_words;
 };
 
-// Append m <= 32 bits (v < 2^m), MSB first; whole 32-bit words are stored
-// big-endian so that the slot holds the stream's bytes in order.
-__device__ __forceinline__ void put_bits(Enc &e, uint64_t v, uint32_t m)
+// A carry that ran past every buffered bit goes into the stored words
+// (big-endian words). Rare: it needs a run of 1 bits over the whole buffer.
+__device__ __noinline__ void carry_into_stored(Enc &e, uint32_t ov)
 {
-    e.acc = (e.acc << m) | v;
-    e.nb += m;
+    for (uint32_t i = e.wp; i > 0 && ov != 0; --i) {
+        if (i - 1 >= e.cap)
+            continue;
+        const uint32_t w = __byte_perm(e.out[i - 1], 0, 0x0123);
+        const uint32_t s = w + ov;
+        ov = (s < w) ? 1u : 0u;
+        e.out[i - 1] = __byte_perm(s, 0, 0x0123);
+    }
+}
+
+// Store the oldest 32 buffered bits once there are 32. Bits above the
+// buffered ones are carries that overflowed it (normally none).
+__device__ __forceinline__ void enc_store_if_full(Enc &e)
+{
     if (e.nb >= 32) {
         e.nb -= 32;
-        uint32_t w = (uint32_t)(e.acc >> e.nb);
-        if (e.nwords < e.cap_words)
-            e.out[e.nwords] = __byte_perm(w, 0, 0x0123);
-        e.nwords++;
+        const uint32_t ov = e.a1 >> e.nb;
+        const uint32_t w = __funnelshift_r(e.a0, e.a1, e.nb);
+        if (ov != 0)
+            carry_into_stored(e, ov);
+        if (e.wp < e.cap)
+            e.out[e.wp] = __byte_perm(w, 0, 0x0123);
+        e.wp++;
+        e.a1 = 0;
+        e.a0 &= (1u << e.nb) - 1u;  // nb < 32 here
     }
 }
 
-// Rare path: more than 32 bits to emit at once (a long pending run).
-__device__ __noinline__ void put_bits_long(Enc &e, uint32_t B, uint32_t n, uint32_t P)
+// One symbol with CDF bounds c0 < c1 (c1 in 1..65536).
+__device__ __forceinline__ void enc_symbol(Enc &e, uint32_t c0, uint32_t c1)
 {
-    uint32_t b0 = B >> (n - 1);
-    put_bits(e, b0, 1);
-    while (P > 0) {
-        uint32_t c = P < 32u ? P : 32u;
-        uint64_t ones = (((uint64_t)1) << c) - 1;
-        put_bits(e, b0 ? 0 : ones, c);
-        P -= c;
-    }
-    if (n > 1)
-        put_bits(e, B & ((1u << (n - 1)) - 1u), n - 1);
+    const uint32_t t0 = scale16(e.d, c0);
+    const uint32_t t1 = scale16(e.d, c1);
+    const uint32_t xs = e.x + t0;
+    const uint32_t cy = (xs < t0) ? 1u : 0u;  // carry out of the window
+    const uint32_t a0c = e.a0 + cy;
+    e.a1 += (a0c < cy) ? 1u : 0u;
+    const uint32_t dn = t1 - t0 - 1u;  // new range - 1
+    const uint32_t hs = xs + dn;       // window of the high end
+    const uint32_t n = __clz(xs ^ hs);
+    const uint32_t k = __clz((~xs | hs) << (n + 1u));
+    const uint32_t S = n + k;
+    e.a1 = __funnelshift_l(a0c, e.a1, S);
+    e.a0 = __funnelshift_l(xs, a0c, S);
+    e.x = xs << S;
+    e.d = __funnelshift_l(0xFFFFFFFFu, dn, S);
+    e.nb += S;
+    enc_store_if_full(e);
 }
 
-// One coder step for the symbol interval [lo, hi) of 2^16 (hi in 1..65536).
-// The renormalisation of the textbook coder runs bit by bit: while low and
-// high share their top bit, emit it (with the pending bits after the
-// first); then, while low = 01.. and high = 10.., drop their second bit and
-// count a pending bit. Both runs are counted here with leading-zero counts:
-// n shared leading bits, then k underflow positions.
-__device__ __forceinline__ void enc_symbol(Enc &e, uint32_t lo, uint32_t hi)
-{
-    uint32_t d = e.high - e.low;  // range - 1
-    uint32_t nlow = e.low + (uint32_t)(((uint64_t)d * lo + lo) >> 16);
-    uint32_t nhigh = e.low + (uint32_t)(((uint64_t)d * hi + hi) >> 16) - 1u;
-    uint32_t n = __clz(nlow ^ nhigh);
-    uint32_t L1 = nlow << n;
-    uint32_t H1 = (nhigh << n) | ((1u << n) - 1u);
-    uint32_t k = __clz(~((L1 & ~H1) << 1));
-    e.low = (L1 << k) & 0x7FFFFFFFu;
-    e.high = (H1 << k) | ((1u << k) - 1u) | 0x80000000u;
-    uint32_t P = e.pending;
-    if (n != 0) {
-        uint32_t B = nlow >> (32u - n);
-        if (P + n <= 32u) {
-            // first bit, P complements of it, then the other n-1 bits: as a
-            // number that is B + (2^P - 1) * 2^(n-1)
-            uint64_t v = (uint64_t)B + (((((uint64_t)1) << P) - 1) << (n - 1));
-            put_bits(e, v, P + n);
-        } else {
-            put_bits_long(e, B, n, P);
-        }
-        e.pending = k;
-    } else {
-        e.pending = P + k;
-    }
-}
-
-// Termination: one more pending bit, then 0 if low < 1/4 else 1, followed
-// by the pending bits; zero-pad and store the last word. Returns the
-// stream length in bits.
+// Termination: the code value is the frame start plus 1/4 of the window
+// (when the textbook window's low end is below 1/4) or plus 1/2, i.e. two
+// more bits, (x >> 30) + 1 with its carry. Stores the last (zero-padded)
+// word and returns the stream length in bits.
 __device__ __forceinline__ uint32_t enc_finish(Enc &e)
 {
-    uint32_t P = e.pending + 1;
-    uint32_t b = e.low >= kQuarter ? 1u : 0u;
-    if (P + 1 <= 32u) {
-        put_bits(e, ((((uint64_t)1) << P) - 1) + b, P + 1);
-    } else {
-        put_bits(e, b, 1);
-        while (P > 0) {
-            uint32_t c = P < 32u ? P : 32u;
-            put_bits(e, b ? 0 : ((((uint64_t)1) << c) - 1), c);
-            P -= c;
-        }
-    }
-    uint32_t bits = e.nwords * 32u + e.nb;
+    const uint32_t w2 = (e.x >> 30) + 1u;
+    const uint32_t cy = w2 >> 2;
+    const uint32_t a0c = e.a0 + cy;
+    e.a1 += (a0c < cy) ? 1u : 0u;
+    e.a1 = __funnelshift_l(a0c, e.a1, 2);
+    e.a0 = (a0c << 2) | (w2 & 3u);
+    e.nb += 2;
+    enc_store_if_full(e);
+    const uint32_t bits = e.wp * 32u + e.nb;
+    const uint32_t ov = __funnelshift_r(e.a0, e.a1, e.nb);  // nb < 32
+    if (ov != 0)
+        carry_into_stored(e, ov);
     if (e.nb) {
-        uint32_t w = (uint32_t)(e.acc << (32u - e.nb));
-        if (e.nwords < e.cap_words)
-            e.out[e.nwords] = __byte_perm(w, 0, 0x0123);
-        e.nwords++;
+        const uint32_t w = e.a0 << (32u - e.nb);
+        if (e.wp < e.cap)
+            e.out[e.wp] = __byte_perm(w, 0, 0x0123);
+        e.wp++;
     }
     return bits;
 }
 
-// ---------------------------------------------------------------- encode
+// Phase A, counting one block of rows: each thread owns W consecutive
+// channels (W = 2: channel pairs with 4-byte loads; W = 1 for narrow rows).
+template <int W>
+__device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, int32_t C,
+                                            int32_t r0, int32_t nr, const float *fac, float fmax,
+                                            uint16_t *table, int32_t Lp, uint8_t *sym_tile)
+{
+    const int32_t units = C / W;
+    for (int32_t p = threadIdx.x; p < units; p += NT) {
+        uint16_t *h0 = table + (size_t)(W * p) * Lp;
+        if (W == 2) {
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(rows) + p;
+            uint16_t *dst = reinterpret_cast<uint16_t *>(sym_tile) + p;
+            uint32_t w[kRowsPerBlock];
+#pragma unroll
+            for (int u = 0; u < kRowsPerBlock; ++u)
+                w[u] = (u < nr) ? __ldg(src + (size_t)(r0 + u) * (C / 2)) : 0u;
+#pragma unroll
+            for (int u = 0; u < kRowsPerBlock; ++u) {
+                if (u < nr) {
+                    const float f = fac[r0 + u];
+                    const uint32_t q0 = quantise(__uint_as_float(w[u] << 16), f, fmax);
+                    const uint32_t q1 = quantise(__uint_as_float(w[u] & 0xFFFF0000u), f, fmax);
+                    h0[q0] += 1;
+                    h0[Lp + q1] += 1;
+                    dst[(size_t)(r0 + u) * (C / 2)] = (uint16_t)(q0 | (q1 << 8));
+                }
+            }
+        } else {
+            const uint16_t *src = rows + p;
+            uint8_t *dst = sym_tile + p;
+            uint32_t w[kRowsPerBlock];
+#pragma unroll
+            for (int u = 0; u < kRowsPerBlock; ++u)
+                w[u] = (u < nr) ? (uint32_t)__ldg(src + (size_t)(r0 + u) * C) : 0u;
+#pragma unroll
+            for (int u = 0; u < kRowsPerBlock; ++u) {
+                if (u < nr) {
+                    const uint32_t q = quantise(__uint_as_float(w[u] << 16), fac[r0 + u], fmax);
+                    h0[q] += 1;
+                    dst[(size_t)(r0 + u) * C] = (uint8_t)q;
+                }
+            }
+        }
+    }
+}
+
+// Phase A, amax of one row (one warp): writes the factor, the scale and
+// raises the non-finite flag.
+__device__ __forceinline__ void row_amax(const uint16_t *__restrict__ row, int32_t C, float fmax,
+                                         float *fac_t, float *amax_t, uint32_t *nonfinite)
+{
+    const int lane = threadIdx.x & 31;
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
+    uint32_t m = 0;
+    for (int v = lane; v < C / 8; v += 32) {
+        const uint4 x = __ldg(r4 + v);
+        m = __vmaxu2(m, x.x & 0x7FFF7FFFu);
+        m = __vmaxu2(m, x.y & 0x7FFF7FFFu);
+        m = __vmaxu2(m, x.z & 0x7FFF7FFFu);
+        m = __vmaxu2(m, x.w & 0x7FFF7FFFu);
+    }
+    m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) {
+        const float a = __uint_as_float(m << 16);
+        float f;
+        if (m >= 0x7F80u) {  // inf or NaN in the row
+            *nonfinite = 1;
+            f = 0.0f;
+        } else {
+            f = (m == 0) ? 0.0f : __fdiv_rn(fmax, a);
+        }
+        *fac_t = f;
+        *amax_t = a;
+    }
+}
 
 __global__ void __launch_bounds__(NT, 3)
-    k_encode_tiles(const uint16_t *__restrict__ kv, const cg_tile_params P, uint8_t *sym_ws,
-                   float *__restrict__ amax_out, uint16_t *__restrict__ cdf_out,
-                   int32_t *__restrict__ lengths, uint8_t *__restrict__ slots,
-                   uint32_t *__restrict__ tile_totals, uint32_t *__restrict__ status)
+    k_encode_tiles(const uint16_t *__restrict__ kv, const cg_tile_params P, int32_t cls_begin,
+                   int32_t cls_count, uint8_t *sym_ws, float *__restrict__ amax_out,
+                   uint16_t *__restrict__ cdf_out, int32_t *__restrict__ lengths,
+                   uint8_t *__restrict__ slots, uint32_t *__restrict__ tile_totals,
+                   uint32_t *__restrict__ status)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    const Tile tl = tile_of(P, blockIdx.x);
+    const Tile tl = tile_of_class(P, cls_begin, cls_count, blockIdx.x);
     const int32_t C = P.C;
     const int32_t N = tl.N, Lp = N + 1;
-    const int32_t M = N / 2 - 1;
-    const float fmax = (float)M;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float fmax = (float)(N / 2 - 1);
+    const int tid = threadIdx.x, warp = tid >> 5;
 
-    // shared layout: table[C][Lp] u16 (histogram, then CDF), fac[256] f32
+    // shared: table[C][Lp] u16 (histogram, then CDF) | fac[256] f32
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
     const uint32_t table_bytes = ((uint32_t)C * Lp * 2u + 15u) & ~15u;
     float *fac = reinterpret_cast<float *>(smem + table_bytes);
@@ -254,79 +357,30 @@ __global__ void __launch_bounds__(NT, 3)
             t4[i] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
+    const uint16_t *rows = kv + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0) * (size_t)C;
+    float *amax_row = amax_out + ((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0;
+    uint8_t *sym_tile = sym_ws + tl.first_stream * (uint64_t)C;
+    const int32_t nblocks = (tl.n + kRowsPerBlock - 1) / kRowsPerBlock;
 
-    const size_t row_stride = (size_t)C;
-    const uint16_t *rows = kv + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0) * row_stride;
-
-    // A1: amax per token (warp per row). |x| on bf16 bits is the bit pattern
-    // with the sign cleared; finite values order like their patterns.
-    for (int t = warp; t < tl.n; t += NT / 32) {
-        const uint4 *r4 = reinterpret_cast<const uint4 *>(rows + (size_t)t * row_stride);
-        uint32_t m = 0;
-        for (int v = lane; v < C / 8; v += 32) {
-            uint4 x = __ldg(r4 + v);
-            m = __vmaxu2(m, x.x & 0x7FFF7FFFu);
-            m = __vmaxu2(m, x.y & 0x7FFF7FFFu);
-            m = __vmaxu2(m, x.z & 0x7FFF7FFFu);
-            m = __vmaxu2(m, x.w & 0x7FFF7FFFu);
-        }
-        m = max(m & 0xFFFFu, m >> 16);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (lane == 0) {
-            float a = __uint_as_float(m << 16);
-            float f;
-            if (m >= 0x7F80u) {  // inf or NaN somewhere in the row
-                nonfinite = 1;
-                f = 0.0f;
-            } else {
-                f = (m == 0) ? 0.0f : __fdiv_rn(fmax, a);
-            }
-            fac[t] = f;
-            amax_out[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + t] = a;
-        }
-    }
+    // A: amax of block 0; then per step, count block b and take the amax
+    // of block b + 1 (one row per warp)
+    if (warp < tl.n)
+        row_amax(rows + (size_t)warp * C, C, fmax, &fac[warp], &amax_row[warp], &nonfinite);
     __syncthreads();
+    for (int32_t b = 0; b < nblocks; ++b) {
+        const int32_t r0 = b * kRowsPerBlock;
+        const int32_t nr = min(kRowsPerBlock, tl.n - r0);
+        if (C / 2 >= NT)
+            count_block<2>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
+        else
+            count_block<1>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
+        const int32_t t = r0 + kRowsPerBlock + warp;
+        if (t < tl.n)
+            row_amax(rows + (size_t)t * C, C, fmax, &fac[t], &amax_row[t], &nonfinite);
+        __syncthreads();
+    }
     if (tid == 0 && nonfinite)
         set_status(status, CG_ERR_NONFINITE);
-
-    // A2: quantise and count. Thread owns channel pairs p = tid + 256 j;
-    // histogram row of channel c is table[c*Lp ...] (Lp odd: the rows of a
-    // warp's 32 consecutive pairs start in 32 different banks).
-    const int32_t npairs = C / 2;
-    uint8_t *sym_tile = sym_ws + tl.first_stream * (uint64_t)C;
-    for (int32_t p = tid; p < npairs; p += NT) {
-        uint16_t *h0 = table + (size_t)(2 * p) * Lp;
-        uint16_t *h1 = h0 + Lp;
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(rows) + p;
-        uint16_t *dst = reinterpret_cast<uint16_t *>(sym_tile) + p;
-        int t = 0;
-        for (; t + 4 <= tl.n; t += 4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                w[u] = __ldg(src + (size_t)(t + u) * (row_stride / 2));
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float f = fac[t + u];
-                uint32_t q0 = quantise(__uint_as_float(w[u] << 16), f, fmax, 2 * M);
-                uint32_t q1 = quantise(__uint_as_float(w[u] & 0xFFFF0000u), f, fmax, 2 * M);
-                h0[q0] += 1;
-                h1[q1] += 1;
-                dst[(size_t)(t + u) * (row_stride / 2)] = (uint16_t)(q0 | (q1 << 8));
-            }
-        }
-        for (; t < tl.n; ++t) {
-            uint32_t w = __ldg(src + (size_t)t * (row_stride / 2));
-            float f = fac[t];
-            uint32_t q0 = quantise(__uint_as_float(w << 16), f, fmax, 2 * M);
-            uint32_t q1 = quantise(__uint_as_float(w & 0xFFFF0000u), f, fmax, 2 * M);
-            h0[q0] += 1;
-            h1[q1] += 1;
-            dst[(size_t)t * (row_stride / 2)] = (uint16_t)(q0 | (q1 << 8));
-        }
-    }
 
     // B: CDF in place. cdf[i] = floor(cum_i * (65536 - N) / n) + i; the floor
     // uses m = ceil(2^32 / n): cum*K < 2^24 and n <= 256 keep the product's
@@ -335,17 +389,14 @@ __global__ void __launch_bounds__(NT, 3)
     {
         const uint64_t inv = ((((uint64_t)1) << 32) + (uint64_t)tl.n - 1) / (uint64_t)tl.n;
         const uint32_t K = 65536u - (uint32_t)N;
-        for (int32_t p = tid; p < npairs; p += NT) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint16_t *row = table + (size_t)(2 * p + h) * Lp;
-                uint32_t cum = 0;
-                for (int32_t i = 0; i <= N; ++i) {
-                    uint32_t cnt = (i < N) ? row[i] : 0u;
-                    uint32_t fl = (uint32_t)(((uint64_t)(cum * K) * inv) >> 32);
-                    row[i] = (uint16_t)(fl + (uint32_t)i);  // 65536 wraps to 0
-                    cum += cnt;
-                }
+        for (int32_t c = tid; c < C; c += NT) {
+            uint16_t *row = table + (size_t)c * Lp;
+            uint32_t cum = 0;
+            for (int32_t i = 0; i <= N; ++i) {
+                const uint32_t cnt = (i < N) ? row[i] : 0u;
+                const uint32_t fl = (uint32_t)(((uint64_t)(cum * K) * inv) >> 32);
+                row[i] = (uint16_t)(fl + (uint32_t)i);  // 65536 wraps to 0
+                cum += cnt;
             }
         }
     }
@@ -363,41 +414,43 @@ __global__ void __launch_bounds__(NT, 3)
     uint32_t nbytes_stream = 0;
     if (tid < tl.n) {
         Enc e;
-        e.low = 0;
-        e.high = 0xFFFFFFFFu;
-        e.pending = 0;
+        e.x = 0;
+        e.d = 0xFFFFFFFFu;
+        e.a0 = e.a1 = 0;
         e.nb = 0;
-        e.acc = 0;
+        e.wp = 0;
+        e.cap = P.slot_stride / 4;
         e.out = reinterpret_cast<uint32_t *>(slots + (tl.first_stream + tid) * (uint64_t)P.slot_stride);
-        e.nwords = 0;
-        e.cap_words = P.slot_stride / 4;
-        const uint8_t *srow = sym_tile + (size_t)tid * C;
+        const uint2 *srow = reinterpret_cast<const uint2 *>(sym_tile + (size_t)tid * C);
+        uint2 next = srow[0];
+        const uint16_t *trow = table;
         for (int32_t c0 = 0; c0 < C; c0 += 8) {
-            uint2 v = *reinterpret_cast<const uint2 *>(srow + c0);
-            const uint16_t *trow = table + (size_t)c0 * Lp;
+            const uint2 v = next;
+            if (c0 + 8 < C)
+                next = srow[(c0 >> 3) + 1];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                uint32_t s = ((j < 4 ? v.x : v.y) >> (8 * (j & 3))) & 0xFFu;
-                uint32_t lo = trow[s];
-                uint32_t hi = (((uint32_t)trow[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
+                const uint32_t s = __byte_perm(j < 4 ? v.x : v.y, 0, 0x4440 + (j & 3));
+                const uint32_t lo = trow[s];
+                const uint32_t hi = (((uint32_t)trow[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
                 enc_symbol(e, lo, hi);
                 trow += Lp;
             }
         }
-        uint32_t bits = enc_finish(e);
+        const uint32_t bits = enc_finish(e);
         nbytes_stream = (bits + 7u) / 8u;
-        if (e.nwords > e.cap_words)
+        if (e.wp > e.cap)
             set_status(status, CG_ERR_CAPACITY);
         lengths[tl.first_stream + tid] = (int32_t)nbytes_stream;
     }
     uint32_t total = 0;
     block_exclusive_scan(nbytes_stream, warp_sums, &total);
     if (tid == 0)
-        tile_totals[blockIdx.x] = total;
+        tile_totals[tl.index] = total;
 }
 
 // Exclusive scan of the per-tile byte totals (one CTA), plus the grand
-// total; when expect is given (decode), the total must equal it.
+// total; when check is set (decode), the total must equal expect.
 __global__ void __launch_bounds__(1024)
     k_scan_tiles(const uint32_t *__restrict__ totals, int32_t ntiles, uint64_t *__restrict__ base,
                  uint64_t *__restrict__ total_out, int check, uint64_t expect,
@@ -410,12 +463,12 @@ __global__ void __launch_bounds__(1024)
         carry_s = 0;
     __syncthreads();
     for (int32_t c0 = 0; c0 < ntiles; c0 += 1024) {
-        int32_t i = c0 + tid;
-        uint64_t v = (i < ntiles) ? totals[i] : 0;
+        const int32_t i = c0 + tid;
+        const uint64_t v = (i < ntiles) ? totals[i] : 0;
         uint64_t x = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            uint64_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
             if (lane >= o)
                 x += y;
         }
@@ -426,15 +479,15 @@ __global__ void __launch_bounds__(1024)
             uint64_t w = wsum[lane];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                uint64_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+                const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
                 if (lane >= o)
                     w += y;
             }
             wsum[lane] = w;
         }
         __syncthreads();
-        uint64_t carry = carry_s;
-        uint64_t excl = carry + (warp ? wsum[warp - 1] : 0) + x - v;
+        const uint64_t carry = carry_s;
+        const uint64_t excl = carry + (warp ? wsum[warp - 1] : 0) + x - v;
         if (i < ntiles)
             base[i] = excl;
         __syncthreads();
@@ -458,16 +511,15 @@ __global__ void __launch_bounds__(NT)
 {
     __shared__ uint32_t warp_sums[NT / 32];
     __shared__ uint32_t offs[NT];
-    const Tile tl = tile_of(P, blockIdx.x);
+    const Tile tl = tile_by_index(P, blockIdx.x);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t len = (tid < tl.n) ? (uint32_t)lengths[tl.first_stream + tid] : 0u;
-    uint32_t off = block_exclusive_scan(len, warp_sums, nullptr);
-    offs[tid] = off;
+    const uint32_t len = (tid < tl.n) ? (uint32_t)lengths[tl.first_stream + tid] : 0u;
+    offs[tid] = block_exclusive_scan(len, warp_sums, nullptr);
     __syncthreads();
     const uint64_t base = tile_base[blockIdx.x];
     for (int i = warp; i < tl.n; i += NT / 32) {
-        uint32_t li = (uint32_t)lengths[tl.first_stream + i];
-        uint64_t dst = base + offs[i];
+        const uint32_t li = (uint32_t)lengths[tl.first_stream + i];
+        const uint64_t dst = base + offs[i];
         if (li > P.slot_stride || dst + li > capacity) {
             if (lane == 0)
                 set_status(status, CG_ERR_CAPACITY);
@@ -487,12 +539,12 @@ __global__ void __launch_bounds__(NT)
                 uint32_t *__restrict__ tile_totals, uint32_t *__restrict__ status)
 {
     __shared__ uint32_t warp_sums[NT / 32];
-    const Tile tl = tile_of(P, blockIdx.x);
+    const Tile tl = tile_by_index(P, blockIdx.x);
     const int tid = threadIdx.x;
     const int32_t maxlen = 2 * P.C + 2;  // 16 bits per symbol + termination
     uint32_t len = 0;
     if (tid < tl.n) {
-        int32_t v = lengths[tl.first_stream + tid];
+        const int32_t v = lengths[tl.first_stream + tid];
         if (v < 1 || v > maxlen)
             set_status(status, CG_ERR_CORRUPT);
         else
@@ -504,75 +556,82 @@ __global__ void __launch_bounds__(NT)
         tile_totals[blockIdx.x] = total;
 }
 
-struct BitReader {
-    const uint8_t *base;
-    uint64_t wa;   // next aligned word to load
-    uint64_t end;  // stream end (bytes past it read as 0)
-    uint64_t buf;  // upcoming bits, MSB first
-    int32_t avail;
-};
-
 __device__ __forceinline__ uint32_t load_word_be(const uint8_t *base, uint64_t wa, uint64_t end)
 {
     if (wa >= end)
         return 0u;
     uint32_t w = __byte_perm(*reinterpret_cast<const uint32_t *>(base + wa), 0, 0x0123);
-    uint64_t nv = end - wa;
+    const uint64_t nv = end - wa;
     if (nv < 4)
         w &= ~(0xFFFFFFFFu >> (8u * (uint32_t)nv));
     return w;
 }
 
-__device__ __forceinline__ void br_refill(BitReader &r)
+// Bit reader: the next `avail` bits of the stream are the top bits of
+// (b1:b0); the bits below them are zero.
+struct Bits {
+    const uint8_t *base;
+    uint64_t wa;   // next aligned word to load
+    uint64_t end;  // stream end (bytes past it read as 0)
+    uint32_t b1, b0;
+    int32_t avail;
+};
+
+__device__ __forceinline__ void bits_refill(Bits &r)
 {
-    if (r.avail <= 32) {
-        r.buf |= (uint64_t)load_word_be(r.base, r.wa, r.end) << (32 - r.avail);
+    if (r.avail <= 32) {  // every valid bit is in b1 and b0 is zero
+        const uint32_t w = load_word_be(r.base, r.wa, r.end);
+        r.b1 |= __funnelshift_rc(w, 0u, (uint32_t)r.avail);  // w >> avail, 0 when avail = 32
+        r.b0 = w << (32 - r.avail);
         r.wa += 4;
         r.avail += 32;
     }
 }
 
-__device__ __forceinline__ void br_init(BitReader &r, const uint8_t *base, uint64_t sb, uint64_t se)
+__device__ __forceinline__ void bits_init(Bits &r, const uint8_t *base, uint64_t sb, uint64_t se)
 {
     r.base = base;
     r.end = se;
     r.wa = sb & ~(uint64_t)3;
-    uint32_t skip = (uint32_t)(sb - r.wa);
-    uint32_t w = load_word_be(base, r.wa, se) << (8u * skip);
-    r.buf = (uint64_t)w << 32;
+    const uint32_t skip = (uint32_t)(sb - r.wa);
+    r.b1 = load_word_be(base, r.wa, se) << (8u * skip);
+    r.b0 = 0;
     r.avail = 32 - 8 * (int32_t)skip;
     r.wa += 4;
-    br_refill(r);
-    br_refill(r);
+    bits_refill(r);
 }
 
-// Take m <= 32 bits.
-__device__ __forceinline__ uint32_t br_take(BitReader &r, uint32_t m)
+// Drop S <= 18 bits.
+__device__ __forceinline__ void bits_skip(Bits &r, uint32_t S)
 {
-    uint32_t v = (uint32_t)((r.buf >> 1) >> (63u - m));
-    r.buf <<= m;
-    r.avail -= (int32_t)m;
-    br_refill(r);
-    return v;
+    r.b1 = __funnelshift_l(r.b0, r.b1, S);
+    r.b0 <<= S;
+    r.avail -= (int32_t)S;
+    bits_refill(r);
 }
 
 __global__ void __launch_bounds__(NT, 3)
-    k_decode_tiles(const cg_tile_params P, const uint8_t *__restrict__ bytestream,
-                   uint64_t stream_bytes, const int32_t *__restrict__ lengths,
-                   const uint16_t *__restrict__ cdf, const float *__restrict__ amax,
-                   const uint64_t *__restrict__ tile_base, uint16_t *__restrict__ kv_out,
-                   uint32_t *__restrict__ status)
+    k_decode_tiles(const cg_tile_params P, int32_t cls_begin, int32_t cls_count,
+                   int32_t bucket_log2, const uint8_t *__restrict__ bytestream, uint64_t stream_bytes,
+                   const int32_t *__restrict__ lengths, const uint16_t *__restrict__ cdf,
+                   const float *__restrict__ amax, const uint64_t *__restrict__ tile_base,
+                   uint16_t *__restrict__ kv_out, uint32_t *__restrict__ status)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t warp_sums[NT / 32];
     __shared__ float deq[64];
     __shared__ uint32_t bad;
-    const Tile tl = tile_of(P, blockIdx.x);
+    const Tile tl = tile_of_class(P, cls_begin, cls_count, blockIdx.x);
     const int32_t C = P.C;
     const int32_t N = tl.N, Lp = N + 1;
     const int32_t M = N / 2 - 1;
     const int tid = threadIdx.x;
+    // shared: table[C][Lp] u16 | lut[C][2^bucket_log2] u8
+    const int32_t nbuckets = 1 << bucket_log2;
+    const uint32_t bshift = 16u - (uint32_t)bucket_log2;
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
+    const uint32_t table_bytes = ((uint32_t)C * Lp * 2u + 15u) & ~15u;
+    uint8_t *lut = smem + table_bytes;
 
     if (tid == 0)
         bad = 0;
@@ -587,18 +646,27 @@ __global__ void __launch_bounds__(NT, 3)
         deq[tid] = __fdiv_rn((float)(tid - M), (float)M);
     uint32_t len = 0;
     if (tid < tl.n) {
-        int32_t v = lengths[tl.first_stream + tid];
+        const int32_t v = lengths[tl.first_stream + tid];
         len = (v > 0) ? (uint32_t)v : 0u;
     }
-    uint32_t off = block_exclusive_scan(len, warp_sums, nullptr);  // has __syncthreads
-    // every CDF row must start at 0, end at 65536 (stored 0) and rise strictly
+    const uint32_t off = block_exclusive_scan(len, warp_sums, nullptr);  // has __syncthreads
+    // validate every row (0, strictly rising, 65536 stored as 0) and build
+    // the bucket table: lut[c][j] = largest s with cdf[s] <= j * 2^bshift
     for (int32_t c = tid; c < C; c += NT) {
         const uint16_t *row = table + (size_t)c * Lp;
         uint32_t ok = (row[0] == 0) && (row[N] == 0);
         for (int32_t i = 1; i < N; ++i)
-            ok &= (row[i] > row[i - 1]);
+            ok &= (row[i] > row[i - 1]) ? 1u : 0u;
         if (!ok)
             bad = 1;
+        uint8_t *lr = lut + (size_t)c * nbuckets;
+        int32_t s = 0;
+        for (int32_t j = 0; j < nbuckets; ++j) {
+            const uint32_t lim = (uint32_t)j << bshift;
+            while (s + 1 < N && row[s + 1] != 0 && (uint32_t)row[s + 1] <= lim)
+                ++s;
+            lr[j] = (uint8_t)s;
+        }
     }
     __syncthreads();
     if (bad) {
@@ -609,7 +677,7 @@ __global__ void __launch_bounds__(NT, 3)
     if (tid >= tl.n)
         return;
 
-    uint64_t sb = tile_base[blockIdx.x] + off;
+    uint64_t sb = tile_base[tl.index] + off;
     uint64_t se = sb + len;
     if (se > stream_bytes) {
         set_status(status, CG_ERR_CORRUPT);
@@ -617,53 +685,72 @@ __global__ void __launch_bounds__(NT, 3)
         if (sb > se)
             sb = se;
     }
-    BitReader br;
-    br_init(br, bytestream, sb, se);
-    uint32_t low = 0, high = 0xFFFFFFFFu;
-    uint32_t value = br_take(br, 32);
+    Bits br;
+    bits_init(br, bytestream, sb, se);
+    // state: x = window of the absolute low end, d = range - 1,
+    // v = code value - low end
+    uint32_t x = 0, d = 0xFFFFFFFFu;
+    uint32_t v = br.b1;
+    bits_skip(br, 16);
+    bits_skip(br, 16);
     const float a = amax[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + tid];
     uint16_t *orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + tid) * (size_t)C;
-    const uint32_t top_step = 1u << (31 - __clz((uint32_t)(N - 1)));
+    const uint16_t *row = table;
+    const uint8_t *lrow = lut;
 
     for (int32_t c0 = 0; c0 < C; c0 += 8) {
         uint32_t packed[4];
-        const uint16_t *row = table + (size_t)c0 * Lp;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            uint32_t d = high - low;
-            uint32_t v = value - low;
-            uint32_t s = 0;
-            for (uint32_t step = top_step; step != 0; step >>= 1) {
-                uint32_t t = s + step;
-                if (t < (uint32_t)N) {
-                    uint32_t cv = row[t];
-                    if ((uint32_t)(((uint64_t)d * cv + cv) >> 16) <= v)
-                        s = t;
-                }
+            // target estimate T ~ (v + 1) * 2^16 / r, then the bucket table
+            const float rf = __uint2float_rz(d) + 1.0f;
+            const float vf = __uint2float_rz(v) + 1.0f;
+            uint32_t te = __float2uint_rz(__fmul_rn(vf, __fdividef(65536.0f, rf)));
+            te = min(te, 65535u);
+            uint32_t s = lrow[te >> bshift];
+            while (s + 1 < (uint32_t)N && (uint32_t)row[s + 1] <= te)
+                ++s;
+            // the coder's exact interval test, t0 <= v < t1, fixes an estimate
+            // that was one off
+            uint32_t c0v = row[s];
+            uint32_t c1v = (((uint32_t)row[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
+            uint32_t t0 = scale16(d, c0v);
+            while (v < t0 && s > 0) {
+                --s;
+                c1v = c0v;
+                c0v = row[s];
+                t0 = scale16(d, c0v);
             }
-            uint32_t lo = row[s];
-            uint32_t hi = (((uint32_t)row[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
-            uint32_t nlow = low + (uint32_t)(((uint64_t)d * lo + lo) >> 16);
-            uint32_t nhigh = low + (uint32_t)(((uint64_t)d * hi + hi) >> 16) - 1u;
-            uint32_t n = __clz(nlow ^ nhigh);
-            uint32_t L1 = nlow << n;
-            uint32_t H1 = (nhigh << n) | ((1u << n) - 1u);
-            uint32_t k = __clz(~((L1 & ~H1) << 1));
-            low = (L1 << k) & 0x7FFFFFFFu;
-            high = (H1 << k) | ((1u << k) - 1u) | 0x80000000u;
-            uint32_t bits = br_take(br, n + k);
-            uint32_t V1 = (value << n) | (bits >> k);
-            value = (V1 & 0x80000000u) | ((V1 << k) & 0x7FFFFFFFu) | (bits & ((1u << k) - 1u));
+            uint32_t dn = scale16(d, c1v) - t0 - 1u;
+            while (v - t0 > dn && s + 1 < (uint32_t)N) {
+                ++s;
+                c0v = c1v;
+                c1v = (((uint32_t)row[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;
+                t0 = scale16(d, c0v);
+                dn = scale16(d, c1v) - t0 - 1u;
+            }
+            // renormalise (see Enc); v takes S new bits
+            const uint32_t xs = x + t0;
+            const uint32_t hs = xs + dn;
+            const uint32_t n = __clz(xs ^ hs);
+            const uint32_t k = __clz((~xs | hs) << (n + 1u));
+            const uint32_t S = n + k;
+            x = xs << S;
+            d = __funnelshift_l(0xFFFFFFFFu, dn, S);
+            v = __funnelshift_l(br.b1, v - t0, S);
+            bits_skip(br, S);
             // dequantise: bf16(fp32((q - MAX) / MAX) * a)
-            float y = __fmul_rn(deq[s], a);
-            uint32_t yb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y));
+            const uint32_t yb =
+                (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(deq[s], a)));
             if (j & 1)
                 packed[j >> 1] |= yb << 16;
             else
                 packed[j >> 1] = yb;
             row += Lp;
+            lrow += nbuckets;
         }
-        *reinterpret_cast<uint4 *>(orow + c0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        *reinterpret_cast<uint4 *>(orow + c0) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
 }
 
@@ -691,6 +778,16 @@ cudaError_t ensure_smem_attributes()
 
 }  // namespace
 
+size_t cg_smem_encode(int32_t C, int32_t bins)
+{
+    return (((size_t)C * (bins + 1) * 2 + 15) & ~(size_t)15) + CG_GROUP_TOKENS * sizeof(float);
+}
+
+size_t cg_smem_decode(int32_t C, int32_t bins, int32_t bucket_log2)
+{
+    return (((size_t)C * (bins + 1) * 2 + 15) & ~(size_t)15) + ((size_t)C << bucket_log2);
+}
+
 const char *cg_kernel_name(int id)
 {
     static const char *names[CG_K_COUNT] = {"k_encode_tiles", "k_scan_tiles(encode)", "k_pack",
@@ -715,8 +812,8 @@ void cg_profiler::end(cudaStream_t s)
     ++used;
 }
 
-int cg_encode_launch_count() { return 3; }
-int cg_decode_launch_count() { return 3; }
+int cg_encode_launch_count(const cg_plan *p) { return (int)p->classes.size() + 2; }
+int cg_decode_launch_count(const cg_plan *p) { return (int)p->classes.size() + 2; }
 
 cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const cg_encoded *out,
                              cudaStream_t stream)
@@ -736,10 +833,12 @@ cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const c
     err = ensure_smem_attributes();
     if (err != cudaSuccess)
         return err;
+    // the tile kernels of all bin classes are timed as one
     p->prof.begin(CG_K_ENCODE_TILES, stream);
-    k_encode_tiles<<<ntiles, NT, p->smem_encode, stream>>>(
-        static_cast<const uint16_t *>(kv), p->tp, sym, out->amax, out->cdf, out->lengths, slots,
-        tile_totals, status);
+    for (const cg_bin_class &cl : p->classes)
+        k_encode_tiles<<<p->tp.ngroups * cl.count, NT, cl.smem_encode, stream>>>(
+            static_cast<const uint16_t *>(kv), p->tp, cl.begin, cl.count, sym, out->amax,
+            out->cdf, out->lengths, slots, tile_totals, status);
     p->prof.end(stream);
     p->prof.begin(CG_K_SCAN_ENCODE, stream);
     k_scan_tiles<<<1, 1024, 0, stream>>>(tile_totals, ntiles, tile_base, total, 0, 0, status);
@@ -775,9 +874,10 @@ cudaError_t cg_launch_decode(const cg_plan *p, const cg_encoded *in, uint64_t st
                                          status);
     p->prof.end(stream);
     p->prof.begin(CG_K_DECODE_TILES, stream);
-    k_decode_tiles<<<ntiles, NT, p->smem_decode, stream>>>(
-        p->tp, in->bytestream, stream_bytes, in->lengths, in->cdf, in->amax, tile_base,
-        static_cast<uint16_t *>(kv_out), status);
+    for (const cg_bin_class &cl : p->classes)
+        k_decode_tiles<<<p->tp.ngroups * cl.count, NT, cl.smem_decode, stream>>>(
+            p->tp, cl.begin, cl.count, cl.bucket_log2, in->bytestream, stream_bytes, in->lengths, in->cdf,
+            in->amax, tile_base, static_cast<uint16_t *>(kv_out), status);
     p->prof.end(stream);
     return cudaGetLastError();
 }

@@ -108,6 +108,7 @@ EDGE = [
     (1, 513, 8, 64, 1000, [(0, 1, 64)], [(0, 1, 4)], "normal"),     # chunk > T
     (2, 64, 8, 512, 64, [(0, 2, 16)], [(0, 2, 16)], "normal"),      # C = 4096 (16 bins)
     (2, 100, 16, 128, 64, [(0, 2, 32)], [(0, 1, 16), (1, 2, 32)], "normal"),  # C = 2048
+    (2, 256, 4, 64, 256, [(0, 2, 32)], [(0, 2, 16)], "bimodal"),    # near-half CDF splits
 ]
 
 
@@ -117,7 +118,11 @@ def _edge_bits(L, T, C, kind, seed):
         b = np.zeros((L, 2, T, C), dtype=np.uint16)
         b[..., ::3] = 0x8000  # -0.0 too
         return b
-    if kind == "constant":
+    if kind == "bimodal":
+        # every value is +-1: symbols 0 and 2*MAX with near-equal counts, so the
+        # coder's interval keeps straddling the middle (long pending runs, carries)
+        x = np.where(rng.random((L, 2, T, C)) < 0.5, -1.0, 1.0)
+    elif kind == "constant":
         x = np.broadcast_to(rng.standard_normal((L, 2, T, 1)), (L, 2, T, C))
     elif kind == "extreme":
         x = rng.standard_normal((L, 2, T, C)) * np.exp(rng.uniform(-80, 80, (L, 2, T, 1)))
