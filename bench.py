@@ -244,7 +244,7 @@ def run_codec(args):
     torch.cuda.set_device(dev)
     name = args.workload
     p, k, v = workload_info(name)
-    L, T, H, D = p["L"], p["T"], p["H"], p["D"]
+    L, T, H, D = p["L"], (args.tokens or p["T"]), p["H"], p["D"]
     C = H * D
     ch = p["chunk_tokens"][0]
 
@@ -253,7 +253,7 @@ def run_codec(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(name, args.cpu_tokens)
 
-    bits = synthetic.generate(name)
+    bits = synthetic.generate(name, num_tokens=T)
     host_kv = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(L, 2, T, H, D)
     kv = host_kv.to(dev)
     codec = cg.Codec(L, T, H, D, ch, k, v, device=dev)
@@ -404,6 +404,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["cachegen", "reference"], default="cachegen")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="truncate the workload to this many tokens (profiling runs)")
     ap.add_argument("--cpu-tokens", type=int, default=2048,
                     help="tokens of the workload in the CPU oracle's bounded sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -170,32 +170,21 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
     tp.slot_stride = (uint32_t)align_up((size_t)C + 16, 16);
     p->max_stream_bytes = align_up((size_t)p->num_streams * (C + 2), 16);
 
-    // launch classes: (kv, layer) pairs grouped by bin count
+    // tile order: (kv, layer) pairs by bin count, largest first
     {
         int32_t k = 0;
-        for (int32_t b = 4; b <= 64; b += 2) {
-            cg_bin_class cl;
-            cl.begin = k;
-            cl.bins = b;
+        p->smem_encode = p->smem_decode = 0;
+        for (int32_t b = 64; b >= 4; b -= 2) {
             for (int kv = 0; kv < 2; ++kv)
                 for (int32_t l = 0; l < L; ++l)
                     if (tp.bins[kv][l] == b)
                         tp.order[k++] = (uint16_t)((kv << 8) | l);
-            cl.count = k - cl.begin;
-            if (cl.count == 0)
-                continue;
-            cl.smem_encode = cg_smem_encode(C, b);
-            // the decoder's bucket table takes what shared memory is left
-            cl.bucket_log2 = 5;
-            while (cl.bucket_log2 > 0 &&
-                   cg_smem_decode(C, b, cl.bucket_log2) > CG_SMEM_LIMIT - 2048)
-                --cl.bucket_log2;
-            cl.smem_decode = cg_smem_decode(C, b, cl.bucket_log2);
-            if (cl.smem_encode > CG_SMEM_LIMIT - 2048 || cl.smem_decode > CG_SMEM_LIMIT - 2048) {
-                delete p;
-                return CG_ERR_UNSUPPORTED;
-            }
-            p->classes.push_back(cl);
+        }
+        p->smem_encode = cg_smem_encode(C, maxb);
+        p->smem_decode = cg_smem_decode(C, maxb);
+        if (p->smem_encode > CG_SMEM_LIMIT - 2048 || p->smem_decode > CG_SMEM_LIMIT - 2048) {
+            delete p;
+            return CG_ERR_UNSUPPORTED;
         }
     }
 

@@ -7,8 +7,9 @@
 // of Witten, Neal & Cleary, CACM 30(6), 1987.
 //
 // Work decomposition: one CTA of 256 threads per tile = (token group,
-// K/V, layer); the tiles of each bin count are one launch, with shared
-// memory sized for that bin count. Encode (then a tile scan and a pack):
+// K/V, layer), all tiles in one launch ordered by bin count, largest
+// first; each CTA branches (uniformly) into a body specialised for 16 or
+// 32 bins, or a generic one. Encode (then a tile scan and a pack):
 //   A  blocks of 8 token rows: warp per row computes amax over the C
 //      channels (16-byte loads; |x| maximum on bf16 bit patterns) and the
 //      row's scale factor; then thread per channel (pair) re-reads the
@@ -21,9 +22,9 @@
 //      channels with the shared-memory CDF rows (see Enc).
 // Pack: block scan of the tile's lengths + the tile's base, then the
 // slots are copied to their packed position. Decode: per tile, the CDF
-// block and a bucket table are staged in shared memory, the lengths are
-// scanned, and each thread decodes one stream and writes the dequantised
-// bf16 row.
+// block is staged in shared memory, the lengths are scanned, and each
+// thread decodes one stream (binary search with the coder's exact
+// comparison) and writes the dequantised bf16 row.
 //
 // No kernel waits on another block, and every loop is bounded by the
 // tile's token and channel counts or the alphabet size.
@@ -79,12 +80,13 @@ __device__ __forceinline__ Tile make_tile(const cg_tile_params &P, int32_t g, in
     return t;
 }
 
-// Tile of block b of a class launch over the pairs order[begin, begin+count).
-__device__ __forceinline__ Tile tile_of_class(const cg_tile_params &P, int32_t begin,
-                                              int32_t count, int32_t b)
+// Tile of block b of the tile grid: pair-major over the (kv, layer) pairs
+// in `order` (largest bin count first), group-minor.
+__device__ __forceinline__ Tile tile_of_order(const cg_tile_params &P, int32_t b)
 {
-    const int32_t g = b / count;
-    const uint32_t kvl = P.order[begin + (b - g * count)];
+    const int32_t i = b / P.ngroups;
+    const int32_t g = b - i * P.ngroups;
+    const uint32_t kvl = P.order[i];
     return make_tile(P, g, (int32_t)(kvl >> 8), (int32_t)(kvl & 0xFFu));
 }
 
@@ -168,16 +170,18 @@ struct Enc {
 };
 
 // A carry that ran past every buffered bit goes into the stored words
-// (big-endian words). Rare: it needs a run of 1 bits over the whole buffer.
-__device__ __noinline__ void carry_into_stored(Enc &e, uint32_t ov)
+// (big-endian words). Rare: it needs a run of 1 bits over the whole
+// buffer. Takes scalars so that the coder state stays in registers.
+__device__ __noinline__ void carry_into_stored(uint32_t *out, uint32_t wp, uint32_t cap,
+                                               uint32_t ov)
 {
-    for (uint32_t i = e.wp; i > 0 && ov != 0; --i) {
-        if (i - 1 >= e.cap)
+    for (uint32_t i = wp; i > 0 && ov != 0; --i) {
+        if (i - 1 >= cap)
             continue;
-        const uint32_t w = __byte_perm(e.out[i - 1], 0, 0x0123);
+        const uint32_t w = __byte_perm(out[i - 1], 0, 0x0123);
         const uint32_t s = w + ov;
         ov = (s < w) ? 1u : 0u;
-        e.out[i - 1] = __byte_perm(s, 0, 0x0123);
+        out[i - 1] = __byte_perm(s, 0, 0x0123);
     }
 }
 
@@ -190,7 +194,7 @@ __device__ __forceinline__ void enc_store_if_full(Enc &e)
         const uint32_t ov = e.a1 >> e.nb;
         const uint32_t w = __funnelshift_r(e.a0, e.a1, e.nb);
         if (ov != 0)
-            carry_into_stored(e, ov);
+            carry_into_stored(e.out, e.wp, e.cap, ov);
         if (e.wp < e.cap)
             e.out[e.wp] = __byte_perm(w, 0, 0x0123);
         e.wp++;
@@ -199,22 +203,32 @@ __device__ __forceinline__ void enc_store_if_full(Enc &e)
     }
 }
 
+// x + t with the carry added into the buffered output (a1:a0).
+__device__ __forceinline__ uint32_t add_with_carry(uint32_t x, uint32_t t, uint32_t &a0,
+                                                   uint32_t &a1)
+{
+    uint32_t xs;
+    asm("add.cc.u32 %0, %3, %4;\n\t"
+        "addc.cc.u32 %1, %1, 0;\n\t"
+        "addc.u32 %2, %2, 0;"
+        : "=r"(xs), "+r"(a0), "+r"(a1)
+        : "r"(x), "r"(t));
+    return xs;
+}
+
 // One symbol with CDF bounds c0 < c1 (c1 in 1..65536).
 __device__ __forceinline__ void enc_symbol(Enc &e, uint32_t c0, uint32_t c1)
 {
     const uint32_t t0 = scale16(e.d, c0);
     const uint32_t t1 = scale16(e.d, c1);
-    const uint32_t xs = e.x + t0;
-    const uint32_t cy = (xs < t0) ? 1u : 0u;  // carry out of the window
-    const uint32_t a0c = e.a0 + cy;
-    e.a1 += (a0c < cy) ? 1u : 0u;
+    const uint32_t xs = add_with_carry(e.x, t0, e.a0, e.a1);
     const uint32_t dn = t1 - t0 - 1u;  // new range - 1
     const uint32_t hs = xs + dn;       // window of the high end
     const uint32_t n = __clz(xs ^ hs);
     const uint32_t k = __clz((~xs | hs) << (n + 1u));
     const uint32_t S = n + k;
-    e.a1 = __funnelshift_l(a0c, e.a1, S);
-    e.a0 = __funnelshift_l(xs, a0c, S);
+    e.a1 = __funnelshift_l(e.a0, e.a1, S);
+    e.a0 = __funnelshift_l(xs, e.a0, S);
     e.x = xs << S;
     e.d = __funnelshift_l(0xFFFFFFFFu, dn, S);
     e.nb += S;
@@ -238,7 +252,7 @@ __device__ __forceinline__ uint32_t enc_finish(Enc &e)
     const uint32_t bits = e.wp * 32u + e.nb;
     const uint32_t ov = __funnelshift_r(e.a0, e.a1, e.nb);  // nb < 32
     if (ov != 0)
-        carry_into_stored(e, ov);
+        carry_into_stored(e.out, e.wp, e.cap, ov);
     if (e.nb) {
         const uint32_t w = e.a0 << (32u - e.nb);
         if (e.wp < e.cap)
@@ -328,17 +342,22 @@ __device__ __forceinline__ void row_amax(const uint16_t *__restrict__ row, int32
     }
 }
 
-__global__ void __launch_bounds__(NT, 3)
-    k_encode_tiles(const uint16_t *__restrict__ kv, const cg_tile_params P, int32_t cls_begin,
-                   int32_t cls_count, uint8_t *sym_ws, float *__restrict__ amax_out,
-                   uint16_t *__restrict__ cdf_out, int32_t *__restrict__ lengths,
-                   uint8_t *__restrict__ slots, uint32_t *__restrict__ tile_totals,
-                   uint32_t *__restrict__ status)
+// One tile of the encoder. NB > 0 fixes the bin count at compile time
+// (16 and 32 are the presets); NB = 0 reads it from the tile.
+template <int NB>
+__device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__restrict__ kv,
+                                            const cg_tile_params &P, uint8_t *sym_ws,
+                                            float *__restrict__ amax_out,
+                                            uint16_t *__restrict__ cdf_out,
+                                            int32_t *__restrict__ lengths,
+                                            uint8_t *__restrict__ slots,
+                                            uint32_t *__restrict__ tile_totals,
+                                            uint32_t *__restrict__ status, uint8_t *smem,
+                                            uint32_t *warp_sums, uint32_t *nonfinite)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const Tile tl = tile_of_class(P, cls_begin, cls_count, blockIdx.x);
     const int32_t C = P.C;
-    const int32_t N = tl.N, Lp = N + 1;
+    const int32_t N = NB > 0 ? NB : tl.N;
+    const int32_t Lp = N + 1;
     const float fmax = (float)(N / 2 - 1);
     const int tid = threadIdx.x, warp = tid >> 5;
 
@@ -346,11 +365,9 @@ __global__ void __launch_bounds__(NT, 3)
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
     const uint32_t table_bytes = ((uint32_t)C * Lp * 2u + 15u) & ~15u;
     float *fac = reinterpret_cast<float *>(smem + table_bytes);
-    __shared__ uint32_t warp_sums[NT / 32];
-    __shared__ uint32_t nonfinite;
 
     if (tid == 0)
-        nonfinite = 0;
+        *nonfinite = 0;
     {
         uint4 *t4 = reinterpret_cast<uint4 *>(table);
         for (uint32_t i = tid; i < table_bytes / 16; i += NT)
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__(NT, 3)
     // A: amax of block 0; then per step, count block b and take the amax
     // of block b + 1 (one row per warp)
     if (warp < tl.n)
-        row_amax(rows + (size_t)warp * C, C, fmax, &fac[warp], &amax_row[warp], &nonfinite);
+        row_amax(rows + (size_t)warp * C, C, fmax, &fac[warp], &amax_row[warp], nonfinite);
     __syncthreads();
     for (int32_t b = 0; b < nblocks; ++b) {
         const int32_t r0 = b * kRowsPerBlock;
@@ -376,10 +393,10 @@ __global__ void __launch_bounds__(NT, 3)
             count_block<1>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
         const int32_t t = r0 + kRowsPerBlock + warp;
         if (t < tl.n)
-            row_amax(rows + (size_t)t * C, C, fmax, &fac[t], &amax_row[t], &nonfinite);
+            row_amax(rows + (size_t)t * C, C, fmax, &fac[t], &amax_row[t], nonfinite);
         __syncthreads();
     }
-    if (tid == 0 && nonfinite)
+    if (tid == 0 && *nonfinite)
         set_status(status, CG_ERR_NONFINITE);
 
     // B: CDF in place. cdf[i] = floor(cum_i * (65536 - N) / n) + i; the floor
@@ -392,6 +409,7 @@ __global__ void __launch_bounds__(NT, 3)
         for (int32_t c = tid; c < C; c += NT) {
             uint16_t *row = table + (size_t)c * Lp;
             uint32_t cum = 0;
+#pragma unroll
             for (int32_t i = 0; i <= N; ++i) {
                 const uint32_t cnt = (i < N) ? row[i] : 0u;
                 const uint32_t fl = (uint32_t)(((uint64_t)(cum * K) * inv) >> 32);
@@ -447,6 +465,27 @@ __global__ void __launch_bounds__(NT, 3)
     block_exclusive_scan(nbytes_stream, warp_sums, &total);
     if (tid == 0)
         tile_totals[tl.index] = total;
+}
+
+__global__ void __launch_bounds__(NT, 3)
+    k_encode_tiles(const uint16_t *__restrict__ kv, const cg_tile_params P, uint8_t *sym_ws,
+                   float *__restrict__ amax_out, uint16_t *__restrict__ cdf_out,
+                   int32_t *__restrict__ lengths, uint8_t *__restrict__ slots,
+                   uint32_t *__restrict__ tile_totals, uint32_t *__restrict__ status)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint32_t warp_sums[NT / 32];
+    __shared__ uint32_t nonfinite;
+    const Tile tl = tile_of_order(P, blockIdx.x);
+    if (tl.N == 16)
+        encode_tile<16>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals,
+                        status, smem, warp_sums, &nonfinite);
+    else if (tl.N == 32)
+        encode_tile<32>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals,
+                        status, smem, warp_sums, &nonfinite);
+    else
+        encode_tile<0>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals,
+                       status, smem, warp_sums, &nonfinite);
 }
 
 // Exclusive scan of the per-tile byte totals (one CTA), plus the grand
@@ -556,48 +595,52 @@ __global__ void __launch_bounds__(NT)
         tile_totals[blockIdx.x] = total;
 }
 
-__device__ __forceinline__ uint32_t load_word_be(const uint8_t *base, uint64_t wa, uint64_t end)
-{
-    if (wa >= end)
-        return 0u;
-    uint32_t w = __byte_perm(*reinterpret_cast<const uint32_t *>(base + wa), 0, 0x0123);
-    const uint64_t nv = end - wa;
-    if (nv < 4)
-        w &= ~(0xFFFFFFFFu >> (8u * (uint32_t)nv));
-    return w;
-}
-
-// Bit reader: the next `avail` bits of the stream are the top bits of
-// (b1:b0); the bits below them are zero.
+// Bit reader over one stream: the next `avail` bits are the top bits of
+// (b1:b0) and the bits below them are zero. Offsets are 32-bit, relative
+// to the aligned word where the stream starts; bytes past the stream's end
+// read as 0.
 struct Bits {
-    const uint8_t *base;
-    uint64_t wa;   // next aligned word to load
-    uint64_t end;  // stream end (bytes past it read as 0)
+    const uint8_t *base;  // aligned start of the stream's first word
+    uint32_t pos;         // next word to load (bytes from base)
+    uint32_t end;         // stream end (bytes from base)
     uint32_t b1, b0;
     int32_t avail;
 };
 
+__device__ __forceinline__ uint32_t bits_word(const Bits &r)
+{
+    if (r.pos >= r.end)
+        return 0u;
+    uint32_t w = __byte_perm(*reinterpret_cast<const uint32_t *>(r.base + r.pos), 0, 0x0123);
+    const uint32_t nv = r.end - r.pos;
+    if (nv < 4)
+        w &= ~(0xFFFFFFFFu >> (8u * nv));
+    return w;
+}
+
 __device__ __forceinline__ void bits_refill(Bits &r)
 {
     if (r.avail <= 32) {  // every valid bit is in b1 and b0 is zero
-        const uint32_t w = load_word_be(r.base, r.wa, r.end);
+        const uint32_t w = bits_word(r);
         r.b1 |= __funnelshift_rc(w, 0u, (uint32_t)r.avail);  // w >> avail, 0 when avail = 32
         r.b0 = w << (32 - r.avail);
-        r.wa += 4;
+        r.pos += 4;
         r.avail += 32;
     }
 }
 
-__device__ __forceinline__ void bits_init(Bits &r, const uint8_t *base, uint64_t sb, uint64_t se)
+__device__ __forceinline__ void bits_init(Bits &r, const uint8_t *bytestream, uint64_t sb,
+                                          uint64_t se)
 {
-    r.base = base;
-    r.end = se;
-    r.wa = sb & ~(uint64_t)3;
-    const uint32_t skip = (uint32_t)(sb - r.wa);
-    r.b1 = load_word_be(base, r.wa, se) << (8u * skip);
+    const uint64_t wa = sb & ~(uint64_t)3;
+    r.base = bytestream + wa;
+    r.pos = 0;
+    r.end = (uint32_t)(se - wa);
+    const uint32_t skip = (uint32_t)(sb - wa);
+    r.b1 = bits_word(r) << (8u * skip);
     r.b0 = 0;
     r.avail = 32 - 8 * (int32_t)skip;
-    r.wa += 4;
+    r.pos = 4;
     bits_refill(r);
 }
 
@@ -610,31 +653,28 @@ __device__ __forceinline__ void bits_skip(Bits &r, uint32_t S)
     bits_refill(r);
 }
 
-__global__ void __launch_bounds__(NT, 3)
-    k_decode_tiles(const cg_tile_params P, int32_t cls_begin, int32_t cls_count,
-                   int32_t bucket_log2, const uint8_t *__restrict__ bytestream, uint64_t stream_bytes,
-                   const int32_t *__restrict__ lengths, const uint16_t *__restrict__ cdf,
-                   const float *__restrict__ amax, const uint64_t *__restrict__ tile_base,
-                   uint16_t *__restrict__ kv_out, uint32_t *__restrict__ status)
+// One tile of the decoder; NB as in encode_tile.
+template <int NB>
+__device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params &P,
+                                            const uint8_t *__restrict__ bytestream,
+                                            uint64_t stream_bytes,
+                                            const int32_t *__restrict__ lengths,
+                                            const uint16_t *__restrict__ cdf,
+                                            const float *__restrict__ amax,
+                                            const uint64_t *__restrict__ tile_base,
+                                            uint16_t *__restrict__ kv_out,
+                                            uint32_t *__restrict__ status, uint8_t *smem,
+                                            uint32_t *warp_sums, float *deq, uint32_t *bad)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ uint32_t warp_sums[NT / 32];
-    __shared__ float deq[64];
-    __shared__ uint32_t bad;
-    const Tile tl = tile_of_class(P, cls_begin, cls_count, blockIdx.x);
     const int32_t C = P.C;
-    const int32_t N = tl.N, Lp = N + 1;
+    const int32_t N = NB > 0 ? NB : tl.N;
+    const int32_t Lp = N + 1;
     const int32_t M = N / 2 - 1;
     const int tid = threadIdx.x;
-    // shared: table[C][Lp] u16 | lut[C][2^bucket_log2] u8
-    const int32_t nbuckets = 1 << bucket_log2;
-    const uint32_t bshift = 16u - (uint32_t)bucket_log2;
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
-    const uint32_t table_bytes = ((uint32_t)C * Lp * 2u + 15u) & ~15u;
-    uint8_t *lut = smem + table_bytes;
 
     if (tid == 0)
-        bad = 0;
+        *bad = 0;
     {
         const uint32_t nb16 = (uint32_t)C * Lp * 2u / 16u;
         const uint4 *src = reinterpret_cast<const uint4 *>(cdf + tl.cdf_base);
@@ -650,26 +690,17 @@ __global__ void __launch_bounds__(NT, 3)
         len = (v > 0) ? (uint32_t)v : 0u;
     }
     const uint32_t off = block_exclusive_scan(len, warp_sums, nullptr);  // has __syncthreads
-    // validate every row (0, strictly rising, 65536 stored as 0) and build
-    // the bucket table: lut[c][j] = largest s with cdf[s] <= j * 2^bshift
+    // every row must start at 0, rise strictly and end at 65536 (stored 0)
     for (int32_t c = tid; c < C; c += NT) {
         const uint16_t *row = table + (size_t)c * Lp;
         uint32_t ok = (row[0] == 0) && (row[N] == 0);
         for (int32_t i = 1; i < N; ++i)
             ok &= (row[i] > row[i - 1]) ? 1u : 0u;
         if (!ok)
-            bad = 1;
-        uint8_t *lr = lut + (size_t)c * nbuckets;
-        int32_t s = 0;
-        for (int32_t j = 0; j < nbuckets; ++j) {
-            const uint32_t lim = (uint32_t)j << bshift;
-            while (s + 1 < N && row[s + 1] != 0 && (uint32_t)row[s + 1] <= lim)
-                ++s;
-            lr[j] = (uint8_t)s;
-        }
+            *bad = 1;
     }
     __syncthreads();
-    if (bad) {
+    if (*bad) {
         if (tid == 0)
             set_status(status, CG_ERR_CORRUPT);
         return;
@@ -696,39 +727,31 @@ __global__ void __launch_bounds__(NT, 3)
     const float a = amax[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + tid];
     uint16_t *orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + tid) * (size_t)C;
     const uint16_t *row = table;
-    const uint8_t *lrow = lut;
+    const uint32_t top_step = 1u << (31 - __clz((uint32_t)(N - 1)));
 
     for (int32_t c0 = 0; c0 < C; c0 += 8) {
         uint32_t packed[4];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            // target estimate T ~ (v + 1) * 2^16 / r, then the bucket table
-            const float rf = __uint2float_rz(d) + 1.0f;
-            const float vf = __uint2float_rz(v) + 1.0f;
-            uint32_t te = __float2uint_rz(__fmul_rn(vf, __fdividef(65536.0f, rf)));
-            te = min(te, 65535u);
-            uint32_t s = lrow[te >> bshift];
-            while (s + 1 < (uint32_t)N && (uint32_t)row[s + 1] <= te)
-                ++s;
-            // the coder's exact interval test, t0 <= v < t1, fixes an estimate
-            // that was one off
-            uint32_t c0v = row[s];
-            uint32_t c1v = (((uint32_t)row[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
-            uint32_t t0 = scale16(d, c0v);
-            while (v < t0 && s > 0) {
-                --s;
-                c1v = c0v;
-                c0v = row[s];
-                t0 = scale16(d, c0v);
+            // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's
+            // own comparison, so the result is exact)
+            uint32_t s = 0;
+            if (NB > 0 && (NB & (NB - 1)) == 0) {
+#pragma unroll
+                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
+                    if (scale16(d, row[s + step]) <= v)
+                        s += step;
+            } else {
+                for (uint32_t step = top_step; step != 0; step >>= 1) {
+                    const uint32_t t = s + step;
+                    if (t < (uint32_t)N && scale16(d, row[t]) <= v)
+                        s = t;
+                }
             }
-            uint32_t dn = scale16(d, c1v) - t0 - 1u;
-            while (v - t0 > dn && s + 1 < (uint32_t)N) {
-                ++s;
-                c0v = c1v;
-                c1v = (((uint32_t)row[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;
-                t0 = scale16(d, c0v);
-                dn = scale16(d, c1v) - t0 - 1u;
-            }
+            const uint32_t c0v = row[s];
+            const uint32_t c1v = (((uint32_t)row[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
+            const uint32_t t0 = scale16(d, c0v);
+            const uint32_t dn = scale16(d, c1v) - t0 - 1u;
             // renormalise (see Enc); v takes S new bits
             const uint32_t xs = x + t0;
             const uint32_t hs = xs + dn;
@@ -747,11 +770,33 @@ __global__ void __launch_bounds__(NT, 3)
             else
                 packed[j >> 1] = yb;
             row += Lp;
-            lrow += nbuckets;
         }
         *reinterpret_cast<uint4 *>(orow + c0) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
+}
+
+__global__ void __launch_bounds__(NT, 3)
+    k_decode_tiles(const cg_tile_params P, const uint8_t *__restrict__ bytestream,
+                   uint64_t stream_bytes, const int32_t *__restrict__ lengths,
+                   const uint16_t *__restrict__ cdf, const float *__restrict__ amax,
+                   const uint64_t *__restrict__ tile_base, uint16_t *__restrict__ kv_out,
+                   uint32_t *__restrict__ status)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint32_t warp_sums[NT / 32];
+    __shared__ float deq[64];
+    __shared__ uint32_t bad;
+    const Tile tl = tile_of_order(P, blockIdx.x);
+    if (tl.N == 16)
+        decode_tile<16>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
+                        status, smem, warp_sums, deq, &bad);
+    else if (tl.N == 32)
+        decode_tile<32>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
+                        status, smem, warp_sums, deq, &bad);
+    else
+        decode_tile<0>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
+                       status, smem, warp_sums, deq, &bad);
 }
 
 // The dynamic shared-memory limit is a per-device function attribute: set
@@ -783,9 +828,9 @@ size_t cg_smem_encode(int32_t C, int32_t bins)
     return (((size_t)C * (bins + 1) * 2 + 15) & ~(size_t)15) + CG_GROUP_TOKENS * sizeof(float);
 }
 
-size_t cg_smem_decode(int32_t C, int32_t bins, int32_t bucket_log2)
+size_t cg_smem_decode(int32_t C, int32_t bins)
 {
-    return (((size_t)C * (bins + 1) * 2 + 15) & ~(size_t)15) + ((size_t)C << bucket_log2);
+    return ((size_t)C * (bins + 1) * 2 + 15) & ~(size_t)15;
 }
 
 const char *cg_kernel_name(int id)
@@ -812,8 +857,8 @@ void cg_profiler::end(cudaStream_t s)
     ++used;
 }
 
-int cg_encode_launch_count(const cg_plan *p) { return (int)p->classes.size() + 2; }
-int cg_decode_launch_count(const cg_plan *p) { return (int)p->classes.size() + 2; }
+int cg_encode_launch_count(const cg_plan *) { return 3; }
+int cg_decode_launch_count(const cg_plan *) { return 3; }
 
 cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const cg_encoded *out,
                              cudaStream_t stream)
@@ -833,12 +878,10 @@ cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const c
     err = ensure_smem_attributes();
     if (err != cudaSuccess)
         return err;
-    // the tile kernels of all bin classes are timed as one
     p->prof.begin(CG_K_ENCODE_TILES, stream);
-    for (const cg_bin_class &cl : p->classes)
-        k_encode_tiles<<<p->tp.ngroups * cl.count, NT, cl.smem_encode, stream>>>(
-            static_cast<const uint16_t *>(kv), p->tp, cl.begin, cl.count, sym, out->amax,
-            out->cdf, out->lengths, slots, tile_totals, status);
+    k_encode_tiles<<<ntiles, NT, p->smem_encode, stream>>>(
+        static_cast<const uint16_t *>(kv), p->tp, sym, out->amax, out->cdf, out->lengths, slots,
+        tile_totals, status);
     p->prof.end(stream);
     p->prof.begin(CG_K_SCAN_ENCODE, stream);
     k_scan_tiles<<<1, 1024, 0, stream>>>(tile_totals, ntiles, tile_base, total, 0, 0, status);
@@ -874,10 +917,9 @@ cudaError_t cg_launch_decode(const cg_plan *p, const cg_encoded *in, uint64_t st
                                          status);
     p->prof.end(stream);
     p->prof.begin(CG_K_DECODE_TILES, stream);
-    for (const cg_bin_class &cl : p->classes)
-        k_decode_tiles<<<p->tp.ngroups * cl.count, NT, cl.smem_decode, stream>>>(
-            p->tp, cl.begin, cl.count, cl.bucket_log2, in->bytestream, stream_bytes, in->lengths, in->cdf,
-            in->amax, tile_base, static_cast<uint16_t *>(kv_out), status);
+    k_decode_tiles<<<ntiles, NT, p->smem_decode, stream>>>(
+        p->tp, in->bytestream, stream_bytes, in->lengths, in->cdf, in->amax, tile_base,
+        static_cast<uint16_t *>(kv_out), status);
     p->prof.end(stream);
     return cudaGetLastError();
 }

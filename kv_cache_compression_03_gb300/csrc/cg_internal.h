@@ -37,17 +37,10 @@ struct cg_tile_params {
     uint32_t pad_;
     uint8_t bins[2][CG_MAX_LAYERS];
     uint32_t cdf_off[2][CG_MAX_LAYERS];  // offset of (kv, l) inside a group block
-    // (kv, layer) pairs sorted by bin count, as (kv << 8) | layer; each bin
-    // count (class) is launched as its own grid with its own shared memory
+    // (kv, layer) pairs as (kv << 8) | layer, largest bin count first: the
+    // tile grid runs through them pair-major, so the heaviest tiles start
+    // first and the tail of the launch is light
     uint16_t order[2 * CG_MAX_LAYERS];
-};
-
-// One launch class: the (kv, layer) pairs order[begin, begin + count) all
-// use `bins` bins.
-struct cg_bin_class {
-    int32_t begin, count, bins;
-    int32_t bucket_log2;  // decoder bucket table: 2^bucket_log2 entries per channel
-    size_t smem_encode, smem_decode;
 };
 
 // Kernel identities for per-kernel timing.
@@ -80,7 +73,7 @@ struct cg_plan {
     // workspace layout (byte offsets)
     size_t ws_tile_totals, ws_tile_base, ws_symbols, ws_slots, ws_bytes;
     size_t max_stream_bytes;
-    std::vector<cg_bin_class> classes;
+    size_t smem_encode, smem_decode;  // dynamic shared memory of the tile kernels
     mutable cg_profiler prof;
 };
 
@@ -93,4 +86,4 @@ int cg_encode_launch_count(const cg_plan *p);
 int cg_decode_launch_count(const cg_plan *p);
 // dynamic shared memory of the tile kernels for C channels and `bins` bins
 size_t cg_smem_encode(int32_t C, int32_t bins);
-size_t cg_smem_decode(int32_t C, int32_t bins, int32_t bucket_log2);
+size_t cg_smem_decode(int32_t C, int32_t bins);
