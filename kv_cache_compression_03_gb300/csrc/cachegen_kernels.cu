@@ -39,7 +39,8 @@
 namespace {
 
 constexpr int NT = CG_TILE_THREADS;
-constexpr int kRowsPerBlock = 8;  // encoder phase A block (one row per warp)
+constexpr int kRowsPerBlock = 8;   // encoder phase A block (one row per warp)
+constexpr int kCountBatch = 8;     // rows whose loads a counting thread keeps in flight
 
 __device__ __forceinline__ void set_status(uint32_t *st, uint32_t code)
 {
@@ -164,8 +165,10 @@ struct Enc {
     uint32_t d;       // range - 1
     uint32_t a0, a1;  // output bits not yet stored: the low nb bits of (a1:a0)
     uint32_t nb;
-    uint32_t wp;      // words stored
+    uint32_t wp;      // words completed
     uint32_t cap;     // slot capacity in words
+    uint32_t hold;    // fast path: the last completed word, not yet stored
+    uint32_t flag;    // fast path: a carry ran past the held word
     uint32_t *out;
 };
 
@@ -185,18 +188,35 @@ __device__ __noinline__ void carry_into_stored(uint32_t *out, uint32_t wp, uint3
     }
 }
 
-// Store the oldest 32 buffered bits once there are 32. Bits above the
-// buffered ones are carries that overflowed it (normally none).
+// Take the oldest 32 buffered bits once there are 32. Bits above the
+// buffered ones are carries that overflowed the buffer (normally none);
+// they belong to the word completed before.
+//  - EXACT: store the word now and push such carries into the stored
+//    words (a rarely taken branch);
+//  - fast path: keep the word in `hold` and store the previously held one,
+//    which takes the carries without a branch; a carry through the whole
+//    held word only raises `flag`, and the stream is then coded again
+//    with the exact path. The fast path has no branch that cannot be
+//    predicated, so the unrolled symbol loop stays one block of code.
+template <bool EXACT>
 __device__ __forceinline__ void enc_store_if_full(Enc &e)
 {
     if (e.nb >= 32) {
         e.nb -= 32;
         const uint32_t ov = e.a1 >> e.nb;
         const uint32_t w = __funnelshift_r(e.a0, e.a1, e.nb);
-        if (ov != 0)
-            carry_into_stored(e.out, e.wp, e.cap, ov);
-        if (e.wp < e.cap)
-            e.out[e.wp] = __byte_perm(w, 0, 0x0123);
+        if (EXACT) {
+            if (ov != 0)
+                carry_into_stored(e.out, e.wp, e.cap, ov);
+            if (e.wp < e.cap)
+                e.out[e.wp] = __byte_perm(w, 0, 0x0123);
+        } else {
+            const uint32_t prev = e.hold + ov;
+            e.flag |= (prev < ov) ? 1u : 0u;
+            if (e.wp > 0 && e.wp - 1 < e.cap)
+                e.out[e.wp - 1] = __byte_perm(prev, 0, 0x0123);
+            e.hold = w;
+        }
         e.wp++;
         e.a1 = 0;
         e.a0 &= (1u << e.nb) - 1u;  // nb < 32 here
@@ -217,6 +237,7 @@ __device__ __forceinline__ uint32_t add_with_carry(uint32_t x, uint32_t t, uint3
 }
 
 // One symbol with CDF bounds c0 < c1 (c1 in 1..65536).
+template <bool EXACT>
 __device__ __forceinline__ void enc_symbol(Enc &e, uint32_t c0, uint32_t c1)
 {
     const uint32_t t0 = scale16(e.d, c0);
@@ -232,13 +253,14 @@ __device__ __forceinline__ void enc_symbol(Enc &e, uint32_t c0, uint32_t c1)
     e.x = xs << S;
     e.d = __funnelshift_l(0xFFFFFFFFu, dn, S);
     e.nb += S;
-    enc_store_if_full(e);
+    enc_store_if_full<EXACT>(e);
 }
 
 // Termination: the code value is the frame start plus 1/4 of the window
 // (when the textbook window's low end is below 1/4) or plus 1/2, i.e. two
-// more bits, (x >> 30) + 1 with its carry. Stores the last (zero-padded)
-// word and returns the stream length in bits.
+// more bits, (x >> 30) + 1 with its carry. Stores what is left (the last
+// word zero-padded) and returns the stream length in bits.
+template <bool EXACT>
 __device__ __forceinline__ uint32_t enc_finish(Enc &e)
 {
     const uint32_t w2 = (e.x >> 30) + 1u;
@@ -248,11 +270,18 @@ __device__ __forceinline__ uint32_t enc_finish(Enc &e)
     e.a1 = __funnelshift_l(a0c, e.a1, 2);
     e.a0 = (a0c << 2) | (w2 & 3u);
     e.nb += 2;
-    enc_store_if_full(e);
+    enc_store_if_full<EXACT>(e);
     const uint32_t bits = e.wp * 32u + e.nb;
     const uint32_t ov = __funnelshift_r(e.a0, e.a1, e.nb);  // nb < 32
-    if (ov != 0)
-        carry_into_stored(e.out, e.wp, e.cap, ov);
+    if (EXACT) {
+        if (ov != 0)
+            carry_into_stored(e.out, e.wp, e.cap, ov);
+    } else if (e.wp > 0) {
+        const uint32_t prev = e.hold + ov;
+        e.flag |= (prev < ov) ? 1u : 0u;
+        if (e.wp - 1 < e.cap)
+            e.out[e.wp - 1] = __byte_perm(prev, 0, 0x0123);
+    }
     if (e.nb) {
         const uint32_t w = e.a0 << (32u - e.nb);
         if (e.wp < e.cap)
@@ -260,6 +289,77 @@ __device__ __forceinline__ uint32_t enc_finish(Enc &e)
         e.wp++;
     }
     return bits;
+}
+
+// Code one token's stream: symbols srow[0..C) with the CDF rows of the
+// shared table. Returns the length in bits; *flag is set when the fast
+// path met a carry it cannot place (then the caller codes it again with
+// EXACT). Reads 16 symbols per load when C is a multiple of 16.
+template <bool EXACT>
+__device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
+                                                const uint16_t *table, int32_t Lp, uint32_t *out,
+                                                uint32_t cap, uint32_t *wp_out, uint32_t *flag)
+{
+    Enc e;
+    e.x = 0;
+    e.d = 0xFFFFFFFFu;
+    e.a0 = e.a1 = 0;
+    e.nb = 0;
+    e.wp = 0;
+    e.cap = cap;
+    e.hold = 0;
+    e.flag = 0;
+    e.out = out;
+    const uint16_t *trow = table;
+    if ((C & 15) == 0) {
+        const uint4 *srow = reinterpret_cast<const uint4 *>(srow8);
+        uint4 next = srow[0];
+        for (int32_t c0 = 0; c0 < C; c0 += 16) {
+            const uint4 v = next;
+            if (c0 + 16 < C)
+                next = srow[(c0 >> 4) + 1];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const uint32_t word = (j < 4) ? v.x : (j < 8) ? v.y : (j < 12) ? v.z : v.w;
+                const uint32_t s = __byte_perm(word, 0, 0x4440 + (j & 3));
+                const uint32_t lo = trow[s];
+                const uint32_t hi = (((uint32_t)trow[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
+                enc_symbol<EXACT>(e, lo, hi);
+                trow += Lp;
+            }
+        }
+    } else {
+        const uint2 *srow = reinterpret_cast<const uint2 *>(srow8);
+        uint2 next = srow[0];
+        for (int32_t c0 = 0; c0 < C; c0 += 8) {
+            const uint2 v = next;
+            if (c0 + 8 < C)
+                next = srow[(c0 >> 3) + 1];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t s = __byte_perm(j < 4 ? v.x : v.y, 0, 0x4440 + (j & 3));
+                const uint32_t lo = trow[s];
+                const uint32_t hi = (((uint32_t)trow[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;
+                enc_symbol<EXACT>(e, lo, hi);
+                trow += Lp;
+            }
+        }
+    }
+    const uint32_t bits = enc_finish<EXACT>(e);
+    *wp_out = e.wp;
+    *flag = e.flag;
+    return bits;
+}
+
+// The exact path, kept out of line: it runs only for streams where the
+// fast path raised its flag. Returns (words << 32) | bits.
+__device__ __noinline__ uint64_t code_stream_exact(const uint8_t *srow8, int32_t C,
+                                                   const uint16_t *table, int32_t Lp,
+                                                   uint32_t *out, uint32_t cap)
+{
+    uint32_t flag = 0, wp = 0;
+    const uint32_t bits = code_stream<true>(srow8, C, table, Lp, out, cap, &wp, &flag);
+    return ((uint64_t)wp << 32) | bits;
 }
 
 // Phase A, counting one block of rows: each thread owns W consecutive
@@ -272,37 +372,40 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
     const int32_t units = C / W;
     for (int32_t p = threadIdx.x; p < units; p += NT) {
         uint16_t *h0 = table + (size_t)(W * p) * Lp;
-        if (W == 2) {
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(rows) + p;
-            uint16_t *dst = reinterpret_cast<uint16_t *>(sym_tile) + p;
-            uint32_t w[kRowsPerBlock];
+        for (int32_t rb = r0; rb < r0 + nr; rb += kCountBatch) {
+            const int32_t nb = min(kCountBatch, r0 + nr - rb);
+            if (W == 2) {
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(rows) + p;
+                uint16_t *dst = reinterpret_cast<uint16_t *>(sym_tile) + p;
+                uint32_t w[kCountBatch];
 #pragma unroll
-            for (int u = 0; u < kRowsPerBlock; ++u)
-                w[u] = (u < nr) ? __ldg(src + (size_t)(r0 + u) * (C / 2)) : 0u;
+                for (int u = 0; u < kCountBatch; ++u)
+                    w[u] = (u < nb) ? __ldg(src + (size_t)(rb + u) * (C / 2)) : 0u;
 #pragma unroll
-            for (int u = 0; u < kRowsPerBlock; ++u) {
-                if (u < nr) {
-                    const float f = fac[r0 + u];
-                    const uint32_t q0 = quantise(__uint_as_float(w[u] << 16), f, fmax);
-                    const uint32_t q1 = quantise(__uint_as_float(w[u] & 0xFFFF0000u), f, fmax);
-                    h0[q0] += 1;
-                    h0[Lp + q1] += 1;
-                    dst[(size_t)(r0 + u) * (C / 2)] = (uint16_t)(q0 | (q1 << 8));
+                for (int u = 0; u < kCountBatch; ++u) {
+                    if (u < nb) {
+                        const float f = fac[rb + u];
+                        const uint32_t q0 = quantise(__uint_as_float(w[u] << 16), f, fmax);
+                        const uint32_t q1 = quantise(__uint_as_float(w[u] & 0xFFFF0000u), f, fmax);
+                        h0[q0] += 1;
+                        h0[Lp + q1] += 1;
+                        dst[(size_t)(rb + u) * (C / 2)] = (uint16_t)(q0 | (q1 << 8));
+                    }
                 }
-            }
-        } else {
-            const uint16_t *src = rows + p;
-            uint8_t *dst = sym_tile + p;
-            uint32_t w[kRowsPerBlock];
+            } else {
+                const uint16_t *src = rows + p;
+                uint8_t *dst = sym_tile + p;
+                uint32_t w[kCountBatch];
 #pragma unroll
-            for (int u = 0; u < kRowsPerBlock; ++u)
-                w[u] = (u < nr) ? (uint32_t)__ldg(src + (size_t)(r0 + u) * C) : 0u;
+                for (int u = 0; u < kCountBatch; ++u)
+                    w[u] = (u < nb) ? (uint32_t)__ldg(src + (size_t)(rb + u) * C) : 0u;
 #pragma unroll
-            for (int u = 0; u < kRowsPerBlock; ++u) {
-                if (u < nr) {
-                    const uint32_t q = quantise(__uint_as_float(w[u] << 16), fac[r0 + u], fmax);
-                    h0[q] += 1;
-                    dst[(size_t)(r0 + u) * C] = (uint8_t)q;
+                for (int u = 0; u < kCountBatch; ++u) {
+                    if (u < nb) {
+                        const uint32_t q = quantise(__uint_as_float(w[u] << 16), fac[rb + u], fmax);
+                        h0[q] += 1;
+                        dst[(size_t)(rb + u) * C] = (uint8_t)q;
+                    }
                 }
             }
         }
@@ -342,6 +445,62 @@ __device__ __forceinline__ void row_amax(const uint16_t *__restrict__ row, int32
     }
 }
 
+// Phase A, amax of one row in two halves: amax_issue starts the row's
+// loads (rows of at most 1024 channels: 4 x 16 bytes per lane) so that they
+// are in flight while the block before is counted; amax_finish reduces them.
+__device__ __forceinline__ void amax_issue(const uint16_t *__restrict__ row, int32_t C,
+                                           bool valid, uint4 (&x)[4])
+{
+    const int lane = threadIdx.x & 31;
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int v = lane + 32 * i;
+        x[i] = (valid && v < C / 8) ? __ldg(r4 + v) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ void amax_finish(const uint4 (&x)[4], bool valid, float fmax,
+                                            float *fac_t, float *amax_t, uint32_t *nonfinite)
+{
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = __vmaxu2(m, x[i].x & 0x7FFF7FFFu);
+        m = __vmaxu2(m, x[i].y & 0x7FFF7FFFu);
+        m = __vmaxu2(m, x[i].z & 0x7FFF7FFFu);
+        m = __vmaxu2(m, x[i].w & 0x7FFF7FFFu);
+    }
+    m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (valid && (threadIdx.x & 31) == 0) {
+        const float a = __uint_as_float(m << 16);
+        float f;
+        if (m >= 0x7F80u) {  // inf or NaN in the row
+            *nonfinite = 1;
+            f = 0.0f;
+        } else {
+            f = (m == 0) ? 0.0f : __fdiv_rn(fmax, a);
+        }
+        *fac_t = f;
+        *amax_t = a;
+    }
+}
+
+// Ask L2 for rows [r, r + nr) of the tile (one contiguous range).
+__device__ __forceinline__ void prefetch_rows(const uint16_t *rows, int32_t C, int32_t r,
+                                              int32_t nr)
+{
+    if (nr <= 0)
+        return;
+    const char *base = reinterpret_cast<const char *>(rows + (size_t)r * C);
+    const uint32_t lines = ((uint32_t)nr * (uint32_t)C * 2u + 127u) / 128u;
+    for (uint32_t i = threadIdx.x; i < lines; i += NT)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 128u * i));
+}
+
 // One tile of the encoder. NB > 0 fixes the bin count at compile time
 // (16 and 32 are the presets); NB = 0 reads it from the tile.
 template <int NB>
@@ -379,21 +538,30 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     uint8_t *sym_tile = sym_ws + tl.first_stream * (uint64_t)C;
     const int32_t nblocks = (tl.n + kRowsPerBlock - 1) / kRowsPerBlock;
 
-    // A: amax of block 0; then per step, count block b and take the amax
-    // of block b + 1 (one row per warp)
+    // A: amax of block 0; then per step, count block b while the loads for
+    // block b + 1's amax are in flight (one row per warp), and ask L2 for
+    // block b + 2
     if (warp < tl.n)
         row_amax(rows + (size_t)warp * C, C, fmax, &fac[warp], &amax_row[warp], nonfinite);
     __syncthreads();
+    const bool pipelined = (C <= 1024);
     for (int32_t b = 0; b < nblocks; ++b) {
         const int32_t r0 = b * kRowsPerBlock;
         const int32_t nr = min(kRowsPerBlock, tl.n - r0);
+        const int32_t r2 = r0 + 2 * kRowsPerBlock;
+        prefetch_rows(rows, C, r2, min(kRowsPerBlock, tl.n - r2));
+        const int32_t ta = r0 + kRowsPerBlock + warp;
+        uint4 xa[4];
+        if (pipelined)
+            amax_issue(rows + (size_t)ta * C, C, ta < tl.n, xa);
         if (C / 2 >= NT)
             count_block<2>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
         else
             count_block<1>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
-        const int32_t t = r0 + kRowsPerBlock + warp;
-        if (t < tl.n)
-            row_amax(rows + (size_t)t * C, C, fmax, &fac[t], &amax_row[t], nonfinite);
+        if (pipelined)
+            amax_finish(xa, ta < tl.n, fmax, &fac[ta], &amax_row[ta], nonfinite);
+        else if (ta < tl.n)
+            row_amax(rows + (size_t)ta * C, C, fmax, &fac[ta], &amax_row[ta], nonfinite);
         __syncthreads();
     }
     if (tid == 0 && *nonfinite)
@@ -431,33 +599,18 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     // C: one stream per token
     uint32_t nbytes_stream = 0;
     if (tid < tl.n) {
-        Enc e;
-        e.x = 0;
-        e.d = 0xFFFFFFFFu;
-        e.a0 = e.a1 = 0;
-        e.nb = 0;
-        e.wp = 0;
-        e.cap = P.slot_stride / 4;
-        e.out = reinterpret_cast<uint32_t *>(slots + (tl.first_stream + tid) * (uint64_t)P.slot_stride);
-        const uint2 *srow = reinterpret_cast<const uint2 *>(sym_tile + (size_t)tid * C);
-        uint2 next = srow[0];
-        const uint16_t *trow = table;
-        for (int32_t c0 = 0; c0 < C; c0 += 8) {
-            const uint2 v = next;
-            if (c0 + 8 < C)
-                next = srow[(c0 >> 3) + 1];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t s = __byte_perm(j < 4 ? v.x : v.y, 0, 0x4440 + (j & 3));
-                const uint32_t lo = trow[s];
-                const uint32_t hi = (((uint32_t)trow[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
-                enc_symbol(e, lo, hi);
-                trow += Lp;
-            }
+        const uint8_t *srow = sym_tile + (size_t)tid * C;
+        uint32_t *out = reinterpret_cast<uint32_t *>(slots + (tl.first_stream + tid) * (uint64_t)P.slot_stride);
+        const uint32_t cap = P.slot_stride / 4;
+        uint32_t wp = 0, flag = 0;
+        uint32_t bits = code_stream<false>(srow, C, table, Lp, out, cap, &wp, &flag);
+        if (flag) {
+            const uint64_t r = code_stream_exact(srow, C, table, Lp, out, cap);
+            bits = (uint32_t)r;
+            wp = (uint32_t)(r >> 32);
         }
-        const uint32_t bits = enc_finish(e);
         nbytes_stream = (bits + 7u) / 8u;
-        if (e.wp > e.cap)
+        if (wp > cap)
             set_status(status, CG_ERR_CAPACITY);
         lengths[tl.first_stream + tid] = (int32_t)nbytes_stream;
     }
