@@ -182,6 +182,17 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
         }
         p->smem_encode = cg_smem_encode(C, maxb);
         p->smem_decode = cg_smem_decode(C, maxb);
+        for (int32_t i = 0; i < k;) {
+            cg_bin_class cl;
+            cl.begin = i;
+            cl.bins = tp.bins[tp.order[i] >> 8][tp.order[i] & 0xFF];
+            while (i < k && tp.bins[tp.order[i] >> 8][tp.order[i] & 0xFF] == cl.bins)
+                ++i;
+            cl.count = i - cl.begin;
+            cl.smem_encode = cg_smem_encode(C, cl.bins);
+            cl.smem_decode = cg_smem_decode(C, cl.bins);
+            p->classes.push_back(cl);
+        }
         if (p->smem_encode > CG_SMEM_LIMIT - 2048 || p->smem_decode > CG_SMEM_LIMIT - 2048) {
             delete p;
             return CG_ERR_UNSUPPORTED;
@@ -205,8 +216,10 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
 
 void cg_plan_destroy(cg_plan *plan)
 {
-    if (plan)
+    if (plan) {
         cg_profile_enable(plan, 0);
+        plan->side.release();
+    }
     delete plan;
 }
 

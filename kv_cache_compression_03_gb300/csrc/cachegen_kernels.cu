@@ -81,13 +81,13 @@ __device__ __forceinline__ Tile make_tile(const cg_tile_params &P, int32_t g, in
     return t;
 }
 
-// Tile of block b of the tile grid: pair-major over the (kv, layer) pairs
-// in `order` (largest bin count first), group-minor.
-__device__ __forceinline__ Tile tile_of_order(const cg_tile_params &P, int32_t b)
+// Tile of block b of a class launch over the pairs order[begin, begin+count)
+// (pair-major, group-minor).
+__device__ __forceinline__ Tile tile_of_class(const cg_tile_params &P, int32_t begin, int32_t b)
 {
     const int32_t i = b / P.ngroups;
     const int32_t g = b - i * P.ngroups;
-    const uint32_t kvl = P.order[i];
+    const uint32_t kvl = P.order[begin + i];
     return make_tile(P, g, (int32_t)(kvl >> 8), (int32_t)(kvl & 0xFFu));
 }
 
@@ -620,25 +620,21 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
         tile_totals[tl.index] = total;
 }
 
-__global__ void __launch_bounds__(NT, 3)
-    k_encode_tiles(const uint16_t *__restrict__ kv, const cg_tile_params P, uint8_t *sym_ws,
-                   float *__restrict__ amax_out, uint16_t *__restrict__ cdf_out,
+// Encoder tiles of one launch class (NB bins; 0 = any), at least MINB
+// CTAs per SM.
+template <int NB, int MINB>
+__global__ void __launch_bounds__(NT, MINB)
+    k_encode_class(const uint16_t *__restrict__ kv, const cg_tile_params P, int32_t cls_begin,
+                   uint8_t *sym_ws, float *__restrict__ amax_out, uint16_t *__restrict__ cdf_out,
                    int32_t *__restrict__ lengths, uint8_t *__restrict__ slots,
                    uint32_t *__restrict__ tile_totals, uint32_t *__restrict__ status)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t warp_sums[NT / 32];
     __shared__ uint32_t nonfinite;
-    const Tile tl = tile_of_order(P, blockIdx.x);
-    if (tl.N == 16)
-        encode_tile<16>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals,
-                        status, smem, warp_sums, &nonfinite);
-    else if (tl.N == 32)
-        encode_tile<32>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals,
-                        status, smem, warp_sums, &nonfinite);
-    else
-        encode_tile<0>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals,
-                       status, smem, warp_sums, &nonfinite);
+    const Tile tl = tile_of_class(P, cls_begin, blockIdx.x);
+    encode_tile<NB>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals, status,
+                    smem, warp_sums, &nonfinite);
 }
 
 // Exclusive scan of the per-tile byte totals (one CTA), plus the grand
@@ -884,6 +880,7 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
 
     for (int32_t c0 = 0; c0 < C; c0 += 8) {
         uint32_t packed[4];
+        float y_even = 0.0f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's
@@ -915,13 +912,15 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
             d = __funnelshift_l(0xFFFFFFFFu, dn, S);
             v = __funnelshift_l(br.b1, v - t0, S);
             bits_skip(br, S);
-            // dequantise: bf16(fp32((q - MAX) / MAX) * a)
-            const uint32_t yb =
-                (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(deq[s], a)));
-            if (j & 1)
-                packed[j >> 1] |= yb << 16;
-            else
-                packed[j >> 1] = yb;
+            // dequantise: bf16(fp32((q - MAX) / MAX) * a), two values per
+            // conversion (each rounded to nearest even on its own)
+            const float y = __fmul_rn(deq[s], a);
+            if (j & 1) {
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(y_even, y);
+                packed[j >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
+            } else {
+                y_even = y;
+            }
             row += Lp;
         }
         *reinterpret_cast<uint4 *>(orow + c0) =
@@ -929,27 +928,49 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
     }
 }
 
-__global__ void __launch_bounds__(NT, 3)
-    k_decode_tiles(const cg_tile_params P, const uint8_t *__restrict__ bytestream,
-                   uint64_t stream_bytes, const int32_t *__restrict__ lengths,
-                   const uint16_t *__restrict__ cdf, const float *__restrict__ amax,
-                   const uint64_t *__restrict__ tile_base, uint16_t *__restrict__ kv_out,
-                   uint32_t *__restrict__ status)
+// Decoder tiles of one launch class (NB bins; 0 = any), at least MINB
+// CTAs per SM.
+template <int NB, int MINB>
+__global__ void __launch_bounds__(NT, MINB)
+    k_decode_class(const cg_tile_params P, int32_t cls_begin,
+                   const uint8_t *__restrict__ bytestream, uint64_t stream_bytes,
+                   const int32_t *__restrict__ lengths, const uint16_t *__restrict__ cdf,
+                   const float *__restrict__ amax, const uint64_t *__restrict__ tile_base,
+                   uint16_t *__restrict__ kv_out, uint32_t *__restrict__ status)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t warp_sums[NT / 32];
     __shared__ float deq[64];
     __shared__ uint32_t bad;
-    const Tile tl = tile_of_order(P, blockIdx.x);
-    if (tl.N == 16)
-        decode_tile<16>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
-                        status, smem, warp_sums, deq, &bad);
-    else if (tl.N == 32)
-        decode_tile<32>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
-                        status, smem, warp_sums, deq, &bad);
-    else
-        decode_tile<0>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
-                       status, smem, warp_sums, deq, &bad);
+    const Tile tl = tile_of_class(P, cls_begin, blockIdx.x);
+    decode_tile<NB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
+                    status, smem, warp_sums, deq, &bad);
+}
+
+// The kernel of each class, by bin count: 16 and 32 have specialised
+// bodies and their own register budgets.
+typedef void (*encode_fn)(const uint16_t *, const cg_tile_params, int32_t, uint8_t *, float *,
+                          uint16_t *, int32_t *, uint8_t *, uint32_t *, uint32_t *);
+typedef void (*decode_fn)(const cg_tile_params, int32_t, const uint8_t *, uint64_t,
+                          const int32_t *, const uint16_t *, const float *, const uint64_t *,
+                          uint16_t *, uint32_t *);
+
+encode_fn encode_kernel(int32_t bins)
+{
+    if (bins == 16)
+        return k_encode_class<16, 3>;
+    if (bins == 32)
+        return k_encode_class<32, 3>;
+    return k_encode_class<0, 3>;
+}
+
+decode_fn decode_kernel(int32_t bins)
+{
+    if (bins == 16)
+        return k_decode_class<16, 4>;
+    if (bins == 32)
+        return k_decode_class<32, 3>;
+    return k_decode_class<0, 3>;
 }
 
 // The dynamic shared-memory limit is a per-device function attribute: set
@@ -964,11 +985,16 @@ cudaError_t ensure_smem_attributes()
     const uint64_t bit = ((uint64_t)1) << (dev & 63);
     if (done.load() & bit)
         return cudaSuccess;
-    err = cudaFuncSetAttribute(k_encode_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               CG_SMEM_LIMIT - 1024);
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(k_decode_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int32_t bins[3] = {16, 32, 0};
+    for (int i = 0; i < 3 && err == cudaSuccess; ++i) {
+        err = cudaFuncSetAttribute(encode_kernel(bins[i]),
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    CG_SMEM_LIMIT - 1024);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(decode_kernel(bins[i]),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       CG_SMEM_LIMIT - 1024);
+    }
     if (err == cudaSuccess)
         done.fetch_or(bit);
     return err;
@@ -1010,8 +1036,81 @@ void cg_profiler::end(cudaStream_t s)
     ++used;
 }
 
-int cg_encode_launch_count(const cg_plan *) { return 3; }
-int cg_decode_launch_count(const cg_plan *) { return 3; }
+int cg_encode_launch_count(const cg_plan *p) { return (int)p->classes.size() + 2; }
+int cg_decode_launch_count(const cg_plan *p) { return (int)p->classes.size() + 2; }
+
+cudaError_t cg_side_stream::ensure()
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (stream != nullptr && device == dev)
+        return cudaSuccess;
+    release();
+    err = cudaStreamCreateWithFlags(&stream, cudaStreamNonBlocking);
+    if (err == cudaSuccess)
+        err = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    if (err == cudaSuccess)
+        err = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    if (err != cudaSuccess) {
+        release();
+        return err;
+    }
+    device = dev;
+    return cudaSuccess;
+}
+
+void cg_side_stream::release()
+{
+    if (stream)
+        cudaStreamDestroy(stream);
+    if (fork)
+        cudaEventDestroy(fork);
+    if (join)
+        cudaEventDestroy(join);
+    stream = nullptr;
+    fork = join = nullptr;
+    device = -1;
+}
+
+namespace {
+
+// Launch every class: the class with the most tiles on the caller's stream,
+// the others on the side stream, forked after the work already enqueued
+// and joined back before anything enqueued later.
+template <typename F>
+cudaError_t launch_classes(const cg_plan *p, cudaStream_t stream, F launch)
+{
+    if (p->classes.size() == 1) {
+        launch(p->classes[0], stream);
+        return cudaGetLastError();
+    }
+    cudaError_t err = p->side.ensure();
+    if (err != cudaSuccess)
+        return err;
+    size_t main = 0;
+    for (size_t i = 1; i < p->classes.size(); ++i)
+        if (p->classes[i].count > p->classes[main].count)
+            main = i;
+    err = cudaEventRecord(p->side.fork, stream);
+    if (err == cudaSuccess)
+        err = cudaStreamWaitEvent(p->side.stream, p->side.fork, 0);
+    if (err != cudaSuccess)
+        return err;
+    for (size_t i = 0; i < p->classes.size(); ++i)
+        if (i != main)
+            launch(p->classes[i], p->side.stream);
+    launch(p->classes[main], stream);
+    err = cudaEventRecord(p->side.join, p->side.stream);
+    if (err == cudaSuccess)
+        err = cudaStreamWaitEvent(stream, p->side.join, 0);
+    if (err != cudaSuccess)
+        return err;
+    return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const cg_encoded *out,
                              cudaStream_t stream)
@@ -1032,10 +1131,14 @@ cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const c
     if (err != cudaSuccess)
         return err;
     p->prof.begin(CG_K_ENCODE_TILES, stream);
-    k_encode_tiles<<<ntiles, NT, p->smem_encode, stream>>>(
-        static_cast<const uint16_t *>(kv), p->tp, sym, out->amax, out->cdf, out->lengths, slots,
-        tile_totals, status);
+    err = launch_classes(p, stream, [&](const cg_bin_class &cl, cudaStream_t s) {
+        encode_kernel(cl.bins)<<<p->tp.ngroups * cl.count, NT, cl.smem_encode, s>>>(
+            static_cast<const uint16_t *>(kv), p->tp, cl.begin, sym, out->amax, out->cdf,
+            out->lengths, slots, tile_totals, status);
+    });
     p->prof.end(stream);
+    if (err != cudaSuccess)
+        return err;
     p->prof.begin(CG_K_SCAN_ENCODE, stream);
     k_scan_tiles<<<1, 1024, 0, stream>>>(tile_totals, ntiles, tile_base, total, 0, 0, status);
     p->prof.end(stream);
@@ -1070,9 +1173,13 @@ cudaError_t cg_launch_decode(const cg_plan *p, const cg_encoded *in, uint64_t st
                                          status);
     p->prof.end(stream);
     p->prof.begin(CG_K_DECODE_TILES, stream);
-    k_decode_tiles<<<ntiles, NT, p->smem_decode, stream>>>(
-        p->tp, in->bytestream, stream_bytes, in->lengths, in->cdf, in->amax, tile_base,
-        static_cast<uint16_t *>(kv_out), status);
+    err = launch_classes(p, stream, [&](const cg_bin_class &cl, cudaStream_t s) {
+        decode_kernel(cl.bins)<<<p->tp.ngroups * cl.count, NT, cl.smem_decode, s>>>(
+            p->tp, cl.begin, in->bytestream, stream_bytes, in->lengths, in->cdf, in->amax,
+            tile_base, static_cast<uint16_t *>(kv_out), status);
+    });
     p->prof.end(stream);
+    if (err != cudaSuccess)
+        return err;
     return cudaGetLastError();
 }

@@ -63,6 +63,23 @@ struct cg_profiler {
     void end(cudaStream_t s);
 };
 
+// One launch class: the (kv, layer) pairs order[begin, begin + count) all
+// use `bins` bins.
+struct cg_bin_class {
+    int32_t begin, count, bins;
+    size_t smem_encode, smem_decode;
+};
+
+// Side stream and fork/join events of a plan, created on first use for
+// the device that is current then (recreated if another device is).
+struct cg_side_stream {
+    int device = -1;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaError_t ensure();
+    void release();
+};
+
 struct cg_plan {
     int32_t L, T, H, D, C, chunk_tokens;
     std::vector<cg_quant_spec> kspecs, vspecs;
@@ -73,7 +90,12 @@ struct cg_plan {
     // workspace layout (byte offsets)
     size_t ws_tile_totals, ws_tile_base, ws_symbols, ws_slots, ws_bytes;
     size_t max_stream_bytes;
-    size_t smem_encode, smem_decode;  // dynamic shared memory of the tile kernels
+    size_t smem_encode, smem_decode;  // dynamic shared memory (largest class)
+    // launch classes, largest bin count first; each class's tiles are one
+    // kernel launch sized for that bin count, and the classes run
+    // concurrently (a side stream forked from and joined to the caller's)
+    std::vector<cg_bin_class> classes;
+    mutable cg_side_stream side;
     mutable cg_profiler prof;
 };
 
