@@ -958,7 +958,7 @@ typedef void (*decode_fn)(const cg_tile_params, int32_t, const uint8_t *, uint64
 encode_fn encode_kernel(int32_t bins)
 {
     if (bins == 16)
-        return k_encode_class<16, 3>;
+        return k_encode_class<16, 4>;
     if (bins == 32)
         return k_encode_class<32, 3>;
     return k_encode_class<0, 3>;
@@ -967,7 +967,7 @@ encode_fn encode_kernel(int32_t bins)
 decode_fn decode_kernel(int32_t bins)
 {
     if (bins == 16)
-        return k_decode_class<16, 4>;
+        return k_decode_class<16, 5>;
     if (bins == 32)
         return k_decode_class<32, 3>;
     return k_decode_class<0, 3>;
