@@ -159,7 +159,8 @@ cg_status cg_encode(const cg_plan *plan, const void *kv, void *workspace, size_t
 
 /* Decode in (device buffers written by cg_encode or cg_deserialize, with
  * stream_bytes bytes of streams; bytestream_capacity must be at least
- * stream_bytes rounded up to 16) into kv_out (device, bf16
+ * stream_bytes rounded up to 16; stream_bytes below the number of
+ * streams is CG_ERR_CORRUPT) into kv_out (device, bf16
  * [L][2][T][H*D], 16-byte aligned) [CG-LMCache §5]. Invalid CDF rows or
  * lengths that do not add up to stream_bytes set CG_ERR_CORRUPT on the
  * device; decoding of a corrupt stream still ends after C symbols per

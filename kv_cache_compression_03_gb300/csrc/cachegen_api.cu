@@ -318,6 +318,8 @@ cg_status cg_decode(const cg_plan *p, const cg_encoded *in, uint64_t stream_byte
     if (!aligned(kv_out, 16) || !aligned(workspace, 256) || !aligned(in->bytestream, 16) ||
         !aligned(in->cdf, 16) || !aligned(in->lengths, 4) || !aligned(in->amax, 4))
         return CG_ERR_INVALID_ARG;
+    if (stream_bytes < p->num_streams)  // every stream has at least one byte
+        return CG_ERR_CORRUPT;
     if (in->bytestream_capacity < align_up((size_t)stream_bytes, 16))
         return CG_ERR_CAPACITY;
     // decode needs only the status block, tile totals and tile bases

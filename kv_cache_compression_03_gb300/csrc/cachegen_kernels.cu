@@ -746,25 +746,22 @@ __global__ void __launch_bounds__(NT)
 
 // Bit reader over one stream: the next `avail` bits are the top bits of
 // (b1:b0) and the bits below them are zero. Offsets are 32-bit, relative
-// to the aligned word where the stream starts; bytes past the stream's end
-// read as 0.
+// to the aligned word where the stream starts. Past the stream's end the
+// reader goes on into whatever follows (the next stream, or the buffer's
+// last word again at its end): a terminated stream decodes to the same
+// symbols whatever bits follow it, so those bits need no masking; loads
+// are only clamped to stay inside the buffer.
 struct Bits {
     const uint8_t *base;  // aligned start of the stream's first word
     uint32_t pos;         // next word to load (bytes from base)
-    uint32_t end;         // stream end (bytes from base)
+    uint32_t lim;         // last loadable word (bytes from base)
     uint32_t b1, b0;
     int32_t avail;
 };
 
 __device__ __forceinline__ uint32_t bits_word(const Bits &r)
 {
-    if (r.pos >= r.end)
-        return 0u;
-    uint32_t w = __byte_perm(*reinterpret_cast<const uint32_t *>(r.base + r.pos), 0, 0x0123);
-    const uint32_t nv = r.end - r.pos;
-    if (nv < 4)
-        w &= ~(0xFFFFFFFFu >> (8u * nv));
-    return w;
+    return __byte_perm(*reinterpret_cast<const uint32_t *>(r.base + min(r.pos, r.lim)), 0, 0x0123);
 }
 
 __device__ __forceinline__ void bits_refill(Bits &r)
@@ -778,13 +775,15 @@ __device__ __forceinline__ void bits_refill(Bits &r)
     }
 }
 
+// sb: the stream's first byte; words may be loaded up to `last` (the
+// buffer's last whole word).
 __device__ __forceinline__ void bits_init(Bits &r, const uint8_t *bytestream, uint64_t sb,
-                                          uint64_t se)
+                                          uint64_t last)
 {
     const uint64_t wa = sb & ~(uint64_t)3;
     r.base = bytestream + wa;
     r.pos = 0;
-    r.end = (uint32_t)(se - wa);
+    r.lim = (uint32_t)(last - wa);
     const uint32_t skip = (uint32_t)(sb - wa);
     r.b1 = bits_word(r) << (8u * skip);
     r.b0 = 0;
@@ -857,16 +856,16 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
     if (tid >= tl.n)
         return;
 
+    // the buffer holds stream_bytes (>= 1) bytes, rounded up to 16 (checked
+    // by the host): its last whole word starts at round4(stream_bytes) - 4
+    const uint64_t last = ((stream_bytes + 3) & ~(uint64_t)3) - 4;
     uint64_t sb = tile_base[tl.index] + off;
-    uint64_t se = sb + len;
-    if (se > stream_bytes) {
+    if (sb + len > stream_bytes) {
         set_status(status, CG_ERR_CORRUPT);
-        se = stream_bytes;
-        if (sb > se)
-            sb = se;
+        sb = min(sb, last);
     }
     Bits br;
-    bits_init(br, bytestream, sb, se);
+    bits_init(br, bytestream, sb, last);
     // state: x = window of the absolute low end, d = range - 1,
     // v = code value - low end
     uint32_t x = 0, d = 0xFFFFFFFFu;
