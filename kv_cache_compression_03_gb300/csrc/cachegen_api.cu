@@ -166,8 +166,10 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
 
     // a stream of C symbols needs at most C + 1 bytes when every coded
     // symbol has frequency >= 256 of 2^16 (true for groups of <= 256
-    // tokens: a symbol that occurs has count >= 1); slots keep C + 16
-    tp.slot_stride = (uint32_t)align_up((size_t)C + 16, 16);
+    // tokens: a symbol that occurs has count >= 1); a slot is a 16-byte pad
+    // (the encoder may write the word before a stream's first one there)
+    // and then room for C + 16 bytes
+    tp.slot_stride = (uint32_t)align_up((size_t)C + 32, 16);
     p->max_stream_bytes = align_up((size_t)p->num_streams * (C + 2), 16);
 
     // tile order: (kv, layer) pairs by bin count, largest first

@@ -211,10 +211,11 @@ __device__ __forceinline__ void enc_store_if_full(Enc &e)
             if (e.wp < e.cap)
                 e.out[e.wp] = __byte_perm(w, 0, 0x0123);
         } else {
+            // out[-1] lies in the slot's pad: the store needs no test for
+            // the first word, only a clamp against the capacity
             const uint32_t prev = e.hold + ov;
             e.flag |= (prev < ov) ? 1u : 0u;
-            if (e.wp > 0 && e.wp - 1 < e.cap)
-                e.out[e.wp - 1] = __byte_perm(prev, 0, 0x0123);
+            e.out[(int32_t)min(e.wp, e.cap) - 1] = __byte_perm(prev, 0, 0x0123);
             e.hold = w;
         }
         e.wp++;
@@ -236,7 +237,8 @@ __device__ __forceinline__ uint32_t add_with_carry(uint32_t x, uint32_t t, uint3
     return xs;
 }
 
-// One symbol with CDF bounds c0 < c1 (c1 in 1..65536).
+// One symbol with CDF bounds c0 < c1 (c1 in 1..65535: the encoder never
+// codes the top symbol, whose upper bound would be 65536).
 template <bool EXACT>
 __device__ __forceinline__ void enc_symbol(Enc &e, uint32_t c0, uint32_t c1)
 {
@@ -276,11 +278,10 @@ __device__ __forceinline__ uint32_t enc_finish(Enc &e)
     if (EXACT) {
         if (ov != 0)
             carry_into_stored(e.out, e.wp, e.cap, ov);
-    } else if (e.wp > 0) {
+    } else {
         const uint32_t prev = e.hold + ov;
         e.flag |= (prev < ov) ? 1u : 0u;
-        if (e.wp - 1 < e.cap)
-            e.out[e.wp - 1] = __byte_perm(prev, 0, 0x0123);
+        e.out[(int32_t)min(e.wp, e.cap) - 1] = __byte_perm(prev, 0, 0x0123);
     }
     if (e.nb) {
         const uint32_t w = e.a0 << (32u - e.nb);
@@ -322,9 +323,9 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
             for (int j = 0; j < 16; ++j) {
                 const uint32_t word = (j < 4) ? v.x : (j < 8) ? v.y : (j < 12) ? v.z : v.w;
                 const uint32_t s = __byte_perm(word, 0, 0x4440 + (j & 3));
-                const uint32_t lo = trow[s];
-                const uint32_t hi = (((uint32_t)trow[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
-                enc_symbol<EXACT>(e, lo, hi);
+                // s <= 2*MAX = N - 2, so cdf[s + 1] is never the top entry
+                // (65536, stored as 0)
+                enc_symbol<EXACT>(e, trow[s], trow[s + 1]);
                 trow += Lp;
             }
         }
@@ -338,9 +339,7 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t s = __byte_perm(j < 4 ? v.x : v.y, 0, 0x4440 + (j & 3));
-                const uint32_t lo = trow[s];
-                const uint32_t hi = (((uint32_t)trow[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;
-                enc_symbol<EXACT>(e, lo, hi);
+                enc_symbol<EXACT>(e, trow[s], trow[s + 1]);
                 trow += Lp;
             }
         }
@@ -600,8 +599,8 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     uint32_t nbytes_stream = 0;
     if (tid < tl.n) {
         const uint8_t *srow = sym_tile + (size_t)tid * C;
-        uint32_t *out = reinterpret_cast<uint32_t *>(slots + (tl.first_stream + tid) * (uint64_t)P.slot_stride);
-        const uint32_t cap = P.slot_stride / 4;
+        uint32_t *out = reinterpret_cast<uint32_t *>(slots + (tl.first_stream + tid) * (uint64_t)P.slot_stride + 16);
+        const uint32_t cap = (P.slot_stride - 16) / 4;
         uint32_t wp = 0, flag = 0;
         uint32_t bits = code_stream<false>(srow, C, table, Lp, out, cap, &wp, &flag);
         if (flag) {
@@ -708,12 +707,12 @@ __global__ void __launch_bounds__(NT)
     for (int i = warp; i < tl.n; i += NT / 32) {
         const uint32_t li = (uint32_t)lengths[tl.first_stream + i];
         const uint64_t dst = base + offs[i];
-        if (li > P.slot_stride || dst + li > capacity) {
+        if (li > P.slot_stride - 16 || dst + li > capacity) {
             if (lane == 0)
                 set_status(status, CG_ERR_CAPACITY);
             continue;
         }
-        const uint8_t *src = slots + (tl.first_stream + i) * (uint64_t)P.slot_stride;
+        const uint8_t *src = slots + (tl.first_stream + i) * (uint64_t)P.slot_stride + 16;
         for (uint32_t b = lane; b < li; b += 32)
             bytestream[dst + b] = src[b];
     }

@@ -33,7 +33,7 @@ struct cg_tile_params {
     int32_t ngroups, ntiles;
     int32_t groups_per_object, full_objects;
     uint64_t cdf_per_group;  // CDF entries of one group (all K/V, layers)
-    uint32_t slot_stride;    // bytes of one stream slot in the workspace
+    uint32_t slot_stride;    // bytes of one stream slot in the workspace (16-byte pad first)
     uint32_t pad_;
     uint8_t bins[2][CG_MAX_LAYERS];
     uint32_t cdf_off[2][CG_MAX_LAYERS];  // offset of (kv, l) inside a group block
