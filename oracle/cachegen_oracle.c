@@ -871,3 +871,80 @@ int32_t orc_max_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------ */
+/* Int8 baseline codec                                                  */
+/* ------------------------------------------------------------------ */
+
+/* The reproduction page ("CacheGen复现项目：面向大模型服务的高效KV缓存压缩与流式传输
+ * 方案", §编解码器模块) quantises KV to 8-bit integers with scale factors and
+ * names no formula. Reading taken: the same symmetric scaling as
+ * [CG-LMCache §2] with MAX = 127 and no offset, one scale per row (K/V,
+ * layer, token): a = max_c |x_c|, f = 127 / a (0 when a = 0),
+ * q = round_half_even(fp32(x * f)) in [-127, 127]; and the inverse of
+ * [CG-LMCache §5] without offset: y = bf16(fp32(fp32(q / 127) * a)). */
+int orc_int8_quantize_row(const uint16_t *x, int32_t C, float *scale, int8_t *q)
+{
+    float a = 0.0f;
+    for (int32_t c = 0; c < C; ++c) {
+        float v = fabsf(bf16_to_float(x[c]));
+        if (!isfinite(v))
+            return ORC_ERR_NONFINITE;
+        if (v > a)
+            a = v;
+    }
+    float f = (a == 0.0f) ? 0.0f : 127.0f / a;
+    for (int32_t c = 0; c < C; ++c) {
+        float y = bf16_to_float(x[c]) * f;
+        int32_t iq = (int32_t)rintf(y);
+        if (iq < -127 || iq > 127)
+            return ORC_ERR_INVALID_ARG; /* cannot happen for finite input */
+        q[c] = (int8_t)iq;
+    }
+    *scale = a;
+    return ORC_OK;
+}
+
+void orc_int8_dequant_row(const int8_t *q, int32_t C, float a, uint16_t *y)
+{
+    for (int32_t c = 0; c < C; ++c) {
+        float t = (float)q[c] / 127.0f;
+        t = t * a;
+        y[c] = float_to_bf16_rne(t);
+    }
+}
+
+/* Whole blob: rows of C channels, row r at kv + r*C; q [rows][C],
+ * scales [rows]. */
+int orc_int8_encode(const uint16_t *kv, int64_t rows, int32_t C, int8_t *q, float *scales,
+                    int32_t nthreads)
+{
+    int st = ORC_OK;
+#ifdef _OPENMP
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (long long r = 0; r < (long long)rows; ++r) {
+        int s = orc_int8_quantize_row(kv + (size_t)r * C, C, &scales[r], q + (size_t)r * C);
+        if (s != ORC_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            st = s;
+        }
+    }
+    return st;
+}
+
+void orc_int8_decode(const int8_t *q, const float *scales, int64_t rows, int32_t C, uint16_t *kv,
+                     int32_t nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (long long r = 0; r < (long long)rows; ++r)
+        orc_int8_dequant_row(q + (size_t)r * C, C, scales[r], kv + (size_t)r * C);
+}

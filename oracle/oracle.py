@@ -92,6 +92,10 @@ def lib() -> ct.CDLL:
                 "orc_serialize": (ct.c_int, [i32, i32, i32, i32, i32, P, i32, P, i32, P, P, P, i64,
                                              P, i64, P, i64]),
                 "orc_max_threads": (i32, []),
+                "orc_int8_quantize_row": (ct.c_int, [P, i32, P, P]),
+                "orc_int8_dequant_row": (None, [P, i32, ct.c_float, P]),
+                "orc_int8_encode": (ct.c_int, [P, i64, i32, P, P, i32]),
+                "orc_int8_decode": (None, [P, P, i64, i32, P, i32]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -306,3 +310,42 @@ def serialize(enc: dict, L, T, H, D, chunk_tokens, kspecs, vspecs) -> bytes:
                                _p(np.ascontiguousarray(enc["cdf"], dtype=np.uint16)), ent,
                                _p(data), sb, _p(out), size), "serialize")
     return out.tobytes()
+
+
+# ---------------------------------------------------------- int8 baseline
+
+def int8_quantize_row(x_bits: np.ndarray):
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    q = np.zeros(x.size, dtype=np.int8)
+    a = ct.c_float(0.0)
+    _check(lib().orc_int8_quantize_row(_p(x), x.size, ct.byref(a), _p(q)), "int8_quantize_row")
+    return float(np.float32(a.value)), q
+
+
+def int8_dequant_row(q: np.ndarray, amax: float) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    y = np.zeros(q.size, dtype=np.uint16)
+    lib().orc_int8_dequant_row(_p(q), q.size, ct.c_float(amax), _p(y))
+    return y
+
+
+def int8_encode(kv_bits: np.ndarray, nthreads: int = 0):
+    """Rows of the last axis: returns (q int8 same shape, scales float32 [rows])."""
+    kv = np.ascontiguousarray(kv_bits, dtype=np.uint16)
+    C = kv.shape[-1]
+    rows = kv.size // C
+    q = np.zeros(kv.shape, dtype=np.int8)
+    sc = np.zeros(rows, dtype=np.float32)
+    _check(lib().orc_int8_encode(_p(kv), rows, C, _p(q), _p(sc),
+                                 nthreads if nthreads > 0 else max_threads()), "int8_encode")
+    return q, sc
+
+
+def int8_decode(q: np.ndarray, scales: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    C = q.shape[-1]
+    out = np.zeros(q.shape, dtype=np.uint16)
+    lib().orc_int8_decode(_p(q), _p(sc), q.size // C, C, _p(out),
+                          nthreads if nthreads > 0 else max_threads())
+    return out
