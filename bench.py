@@ -228,6 +228,87 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU
 
+def rel_rmse(x, y) -> float:
+    """||y - x|| / ||x|| over a whole bf16 blob, one layer at a time."""
+    num = den = 0.0
+    for l in range(x.shape[0]):
+        xf = x[l].float()
+        num += float((y[l].float() - xf).pow(2).sum())
+        den += float(xf.pow(2).sum())
+    return (num / den) ** 0.5 if den > 0 else 0.0
+
+
+TRANSFER_MBPS = (100, 500, 1000)
+
+
+def transfer_model(raw: int, sizes: dict, decode_ms: dict):
+    """Seconds to move one blob over a link of 100/500/1000 Mbit/s and
+    decode it: bytes * 8 / bandwidth, plus the measured GPU decode time
+    (none for raw bf16)."""
+    out = {"bandwidth_mbps": list(TRANSFER_MBPS)}
+    for key, nbytes in [("raw", raw)] + list(sizes.items()):
+        dec_s = decode_ms.get(key, 0.0) * 1e-3
+        out[key + "_s"] = [round(nbytes * 8 / (bw * 1e6) + dec_s, 4) for bw in TRANSFER_MBPS]
+    return out
+
+
+def measure_baselines(cg, kv, cg_out, raw, container, t_dec_ms, peak, stream, dev, args):
+    """The comparison codecs on the same input, after the timed region: the
+    int8 + per-row-scale codec (its own encode and decode loops, CUDA events
+    on the launch stream) and naive serialisation (the raw bytes); the
+    reconstruction error of each lossy codec; and the transfer-time model."""
+    import torch
+    L, _, T, H, D = kv.shape
+    C = H * D
+    rows = 2 * L * T
+    q = torch.empty(rows * C, dtype=torch.int8, device=dev)
+    scales = torch.empty(rows, dtype=torch.float32, device=dev)
+    status = torch.empty(16, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(kv)
+
+    def enc8():
+        cg.cg_int8_encode(kv, rows, C, q, scales, status, stream)
+
+    def dec8():
+        cg.cg_int8_decode(q, scales, rows, C, y, stream)
+
+    for _ in range(max(args.warmup, 1)):
+        enc8()
+        dec8()
+    st, _ = cg.cg_last_device_error(None, status, stream)
+    assert st == cg.CG_OK, st
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for _ in range(args.steps):
+        enc8()
+    ev[1].record(stream)
+    for _ in range(args.steps):
+        dec8()
+    ev[2].record(stream)
+    torch.cuda.synchronize(dev)
+    t_e = ev[0].elapsed_time(ev[1]) / args.steps
+    t_d = ev[1].elapsed_time(ev[2]) / args.steps
+    int8_bytes = rows * C + 4 * rows
+    alg = raw + int8_bytes
+    int8 = {"encode_gbs": round(raw / (t_e * 1e-3) / 1e9, 2),
+            "decode_gbs": round(raw / (t_d * 1e-3) / 1e9, 2),
+            "encode_ms": round(t_e, 4), "decode_ms": round(t_d, 4),
+            "encode_hbm_frac": round(alg / (t_e * 1e-3) / 1e9 / peak, 4),
+            "decode_hbm_frac": round(alg / (t_d * 1e-3) / 1e9 / peak, 4),
+            "compression_ratio": round(raw / int8_bytes, 4), "bytes": int(int8_bytes),
+            "rel_rmse": round(rel_rmse(kv, y), 6),
+            "kernels": ["k_int8_encode", "k_int8_decode"]}
+    return {
+        "int8": int8,
+        "naive": {"compression_ratio": 1.0, "bytes": int(raw), "rel_rmse": 0.0},
+        "cachegen": {"compression_ratio": round(raw / container, 4), "bytes": int(container),
+                     "rel_rmse": round(rel_rmse(kv, cg_out), 6)},
+        "transfer_model": transfer_model(raw, {"cachegen": container, "int8": int8_bytes},
+                                         {"cachegen": t_dec_ms, "int8": t_d}),
+    }
+
+
 def run_codec(args):
     import numpy as np
     import torch
@@ -362,6 +443,10 @@ def run_codec(args):
                "steps": n_e2e, "path": "pinned host kv -> H2D -> cg_encode -> cg_serialize "
                "(D2H container) -> cg_deserialize (H2D) -> cg_decode -> D2H kv"}
 
+    baselines = None
+    if not args.no_baselines:
+        baselines = measure_baselines(cg, kv, out, raw, container, t_dec, peak, stream, dev, args)
+
     if rank != 0:
         return 0
     clocks = clk.summary()
@@ -387,6 +472,7 @@ def run_codec(args):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "baselines": baselines,
         "clocks": clocks,
         "gpu_launches": int(launches_per_step * args.steps),
     }
@@ -410,6 +496,8 @@ def main():
                     help="tokens of the workload in the CPU oracle's bounded sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-baselines", action="store_true",
+                    help="skip the int8/naive comparison codecs and the transfer-time model")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -101,7 +101,8 @@ typedef enum cg_status {
     CG_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size */
     CG_ERR_SPEC = 2,        /* spec ranges do not tile [0, L) or bad bins */
     CG_ERR_CAPACITY = 3,    /* an output buffer is too small */
-    CG_ERR_NONFINITE = 4,   /* the input holds inf or NaN */
+    CG_ERR_NONFINITE = 4,   /* the input holds inf or NaN, or a row too
+                               small for a finite scale factor */
     CG_ERR_CORRUPT = 5,     /* a container or its tables are inconsistent */
     CG_ERR_TIMEOUT = 6,     /* reserved: a bounded device wait gave up */
     CG_ERR_CUDA = 7,        /* a CUDA runtime call failed */
@@ -169,8 +170,10 @@ cg_status cg_decode(const cg_plan *plan, const cg_encoded *in, uint64_t stream_b
                     void *workspace, size_t workspace_bytes, void *kv_out, cg_stream_t stream);
 
 /* Wait for stream, then read the device status word and the total stream
- * bytes of the last cg_encode/cg_decode that used this workspace.
- * Either output may be NULL. Returns CG_ERR_CUDA if the copy fails. */
+ * bytes of the last cg_encode/cg_decode that used this workspace (or the
+ * status block of cg_encode_noalloc or cg_int8_encode; plan may be NULL,
+ * the block's layout does not depend on it). Either output may be NULL.
+ * Returns CG_ERR_CUDA if the copy fails. */
 cg_status cg_last_device_error(const cg_plan *plan, const void *workspace, cg_status *status,
                                uint64_t *stream_bytes, cg_stream_t stream);
 
@@ -224,6 +227,37 @@ cg_status cg_deserialize(const cg_plan *plan, const void *host_in, size_t len,
  * serialise them. Asynchronous on stream. */
 cg_status cg_encode_noalloc(const cg_plan *plan, const void *kv, const cg_encoded *out,
                             void *status_out, cg_stream_t stream);
+
+/* Int8 baseline codec, the comparison point for the ratio and throughput
+ * of the codec above. "CacheGen复现项目：面向大模型服务的高效KV缓存压缩与流式传输
+ * 方案" (§编解码器模块) quantises KV to 8-bit integers with scale factors
+ * and gives no formula; this library reads it as the symmetric scaling of
+ * [CG-LMCache §2] with MAX = 127 and no offset, one scale per row:
+ *   a = max_c |x_c|; f = 127 / a (fp32, f = 0 when a = 0);
+ *   q = round_half_even(fp32(x * f)) in [-127, 127]  (int8)
+ *   y = bf16_rne(fp32(fp32(q / 127) * a))
+ * A row is C = channels bf16 values; for a KV cache, rows are the
+ * (layer, K/V, token) rows of kv[L][2][T][H*D] in memory order, so
+ * rows = 2*L*T and channels = H*D.
+ *
+ * cg_int8_encode: kv (device, bf16 [rows][channels], 16-byte aligned) into
+ * q_out (device, int8 [rows][channels], 8-byte aligned) and scales_out
+ * (device, fp32 [rows], the a of each row). status_out (device, 16 bytes,
+ * 16-byte aligned) is cleared by the call; a row holding inf/NaN, or one
+ * so small (a below about 2^-121) that 127 / a overflows fp32, sets its
+ * first word to CG_ERR_NONFINITE (that row's q are then meaningless); read
+ * it with cg_last_device_error(NULL, status_out, ...). channels is a
+ * multiple of 8 up to 4096 (CG_ERR_INVALID_ARG, CG_ERR_UNSUPPORTED above);
+ * rows = 0 only clears the status. Asynchronous on stream.
+ *
+ * cg_int8_decode: q and scales (device, as written by cg_int8_encode) into
+ * kv_out (device, bf16 [rows][channels], 16-byte aligned). Every byte value
+ * decodes (0x80, never written by the encoder, gives -128/127 * a).
+ * Asynchronous on stream. */
+cg_status cg_int8_encode(const void *kv, int64_t rows, int32_t channels, void *q_out,
+                         float *scales_out, void *status_out, cg_stream_t stream);
+cg_status cg_int8_decode(const void *q, const float *scales, int64_t rows, int32_t channels,
+                         void *kv_out, cg_stream_t stream);
 
 /* Per-kernel timing, for profiling. When enabled, each kernel that
  * cg_encode/cg_decode enqueue is bracketed by two CUDA events on the launch

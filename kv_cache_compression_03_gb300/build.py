@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libcachegen.so")
 
-SOURCES = ["cachegen_kernels.cu", "cachegen_api.cu", "cachegen_noalloc.cu"]
+SOURCES = ["cachegen_kernels.cu", "cachegen_api.cu", "cachegen_noalloc.cu", "cachegen_int8.cu"]
 HEADERS = [os.path.join(CSRC, "cg_internal.h"), os.path.join(INCLUDE, "cachegen.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

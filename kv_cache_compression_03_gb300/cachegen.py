@@ -93,6 +93,8 @@ def load(build_if_missing: bool = True) -> ct.CDLL:
             "cg_deserialize": (st, [P, P, sz, ct.POINTER(cg_encoded), P]),
             "cg_status_string": (ct.c_char_p, [st]),
             "cg_encode_noalloc": (st, [P, P, ct.POINTER(cg_encoded), P, P]),
+            "cg_int8_encode": (st, [P, ct.c_int64, ct.c_int32, P, P, P, P]),
+            "cg_int8_decode": (st, [P, P, ct.c_int64, ct.c_int32, P, P]),
             "cg_profile_enable": (st, [P, ct.c_int32]),
             "cg_profile_read": (st, [P, ct.POINTER(cg_kernel_profile), ct.c_int32,
                                      ct.POINTER(ct.c_int32)]),
@@ -188,11 +190,59 @@ def cg_decode(plan, bytestream, lengths, cdf, amax, stream_bytes, workspace, kv_
                             ct.c_void_p(_ptr(kv_out)), _stream_handle(stream)), "cg_decode")
 
 
+def cg_int8_encode(kv, rows, channels, q_out, scales_out, status_out, stream=None) -> None:
+    """Int8 baseline encode (include/cachegen.h): kv bf16 [rows][channels]
+    into q_out int8 [rows][channels] and scales_out fp32 [rows]; status_out
+    (>= 16 bytes) gets the device status, read with
+    cg_last_device_error(None, status_out)."""
+    _check(load().cg_int8_encode(ct.c_void_p(_ptr(kv)), int(rows), int(channels),
+                                 ct.c_void_p(_ptr(q_out)), ct.c_void_p(_ptr(scales_out)),
+                                 ct.c_void_p(_ptr(status_out)), _stream_handle(stream)),
+           "cg_int8_encode")
+
+
+def cg_int8_decode(q, scales, rows, channels, kv_out, stream=None) -> None:
+    """Int8 baseline decode: q int8 [rows][channels] and scales fp32 [rows]
+    into kv_out bf16 [rows][channels]."""
+    _check(load().cg_int8_decode(ct.c_void_p(_ptr(q)), ct.c_void_p(_ptr(scales)), int(rows),
+                                 int(channels), ct.c_void_p(_ptr(kv_out)), _stream_handle(stream)),
+           "cg_int8_decode")
+
+
+def int8_encode(kv, stream=None, sync: bool = True):
+    """Int8 baseline encode of a contiguous bf16 cuda tensor whose last
+    dimension is the row (a KV cache [L, 2, T, H, D] is taken as rows of
+    H*D). Returns (q int8 of kv's shape, scales fp32 [rows], status tensor);
+    with sync, a device error is raised."""
+    import torch
+    assert kv.dtype == torch.bfloat16 and kv.is_cuda and kv.is_contiguous()
+    C = kv.shape[-1] if kv.dim() != 5 else kv.shape[-2] * kv.shape[-1]
+    rows = kv.numel() // C if C else 0
+    q = torch.empty(kv.shape, dtype=torch.int8, device=kv.device)
+    scales = torch.empty(rows, dtype=torch.float32, device=kv.device)
+    status = torch.empty(16, dtype=torch.uint8, device=kv.device)
+    cg_int8_encode(kv, rows, C, q, scales, status, stream)
+    if sync:
+        st, _ = cg_last_device_error(None, status, stream)
+        _check(st, "cg_int8_encode (device)")
+    return q, scales, status
+
+
+def int8_decode(q, scales, stream=None):
+    """Int8 baseline decode: the bf16 tensor of q's shape."""
+    import torch
+    C = q.shape[-1] if q.dim() != 5 else q.shape[-2] * q.shape[-1]
+    rows = q.numel() // C if C else 0
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    cg_int8_decode(q, scales, rows, C, out, stream)
+    return out
+
+
 def cg_last_device_error(plan, workspace, stream=None):
     """Wait for the stream; return (device status, total stream bytes)."""
     st = ct.c_int(0)
     tot = ct.c_uint64(0)
-    _check(load().cg_last_device_error(ct.c_void_p(plan), ct.c_void_p(_ptr(workspace)),
+    _check(load().cg_last_device_error(ct.c_void_p(plan or 0), ct.c_void_p(_ptr(workspace)),
                                        ct.byref(st), ct.byref(tot), _stream_handle(stream)),
            "cg_last_device_error")
     return st.value, tot.value

@@ -133,11 +133,26 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
 // ------------------------------------------------------------ quantiser
 
 // q = round_half_even(fp32(fp32(x * f) + MAX)). For finite rows q lies in
-// [0, 2*MAX]; rows holding inf/NaN get f = 0, and the conversion of NaN
-// gives 0, so q stays in range for them too (they are reported separately).
+// [0, 2*MAX]; rows without a usable factor get f = 0 (row_factor), and the
+// conversion of NaN gives 0, so q stays in range for them too (they are
+// reported separately).
 __device__ __forceinline__ uint32_t quantise(float x, float f, float fmax)
 {
     return (uint32_t)__float2int_rn(__fadd_rn(__fmul_rn(x, f), fmax));
+}
+
+// Scale factor MAX / a of a row whose largest |x| has bf16 bits m. A row
+// holding inf/NaN, or one so small (a below about 2^-124) that MAX / a
+// overflows fp32, has no usable factor: it gets f = 0 and raises the
+// non-finite flag, which keeps its symbols in range.
+__device__ __forceinline__ float row_factor(uint32_t m, float fmax, uint32_t *nonfinite)
+{
+    float f = (m == 0) ? 0.0f : __fdiv_rn(fmax, __uint_as_float(m << 16));
+    if (m >= 0x7F80u || isinf(f)) {
+        *nonfinite = 1;
+        f = 0.0f;
+    }
+    return f;
 }
 
 // floor(r * c / 2^16) for r = d + 1 <= 2^32 and c <= 65536, kept mod 2^32
@@ -431,16 +446,8 @@ __device__ __forceinline__ void row_amax(const uint16_t *__restrict__ row, int32
     for (int o = 16; o > 0; o >>= 1)
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (lane == 0) {
-        const float a = __uint_as_float(m << 16);
-        float f;
-        if (m >= 0x7F80u) {  // inf or NaN in the row
-            *nonfinite = 1;
-            f = 0.0f;
-        } else {
-            f = (m == 0) ? 0.0f : __fdiv_rn(fmax, a);
-        }
-        *fac_t = f;
-        *amax_t = a;
+        *fac_t = row_factor(m, fmax, nonfinite);
+        *amax_t = __uint_as_float(m << 16);
     }
 }
 
@@ -475,16 +482,8 @@ __device__ __forceinline__ void amax_finish(const uint4 (&x)[4], bool valid, flo
     for (int o = 16; o > 0; o >>= 1)
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (valid && (threadIdx.x & 31) == 0) {
-        const float a = __uint_as_float(m << 16);
-        float f;
-        if (m >= 0x7F80u) {  // inf or NaN in the row
-            *nonfinite = 1;
-            f = 0.0f;
-        } else {
-            f = (m == 0) ? 0.0f : __fdiv_rn(fmax, a);
-        }
-        *fac_t = f;
-        *amax_t = a;
+        *fac_t = row_factor(m, fmax, nonfinite);
+        *amax_t = __uint_as_float(m << 16);
     }
 }
 

@@ -166,6 +166,10 @@ int orc_quantize_row(const uint16_t *x, int32_t C, int32_t bins, float *amax_out
             a = v;
     }
     float f = (a == 0.0f) ? 0.0f : (float)M / a;
+    /* Reading: a row so small that MAX / a overflows fp32 (a below about
+     * 2^-124) has no finite scale factor; it is rejected like inf/NaN. */
+    if (!isfinite(f))
+        return ORC_ERR_NONFINITE;
     for (int32_t c = 0; c < C; ++c) {
         float y = bf16_to_float(x[c]) * f;
         y = y + (float)M;
@@ -894,6 +898,8 @@ int orc_int8_quantize_row(const uint16_t *x, int32_t C, float *scale, int8_t *q)
             a = v;
     }
     float f = (a == 0.0f) ? 0.0f : 127.0f / a;
+    if (!isfinite(f)) /* as in orc_quantize_row */
+        return ORC_ERR_NONFINITE;
     for (int32_t c = 0; c < C; ++c) {
         float y = bf16_to_float(x[c]) * f;
         int32_t iq = (int32_t)rintf(y);

@@ -1,0 +1,29 @@
+"""Host-side arithmetic of the bench: the transfer-time model and the
+relative reconstruction error, on CPU."""
+import os
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def test_transfer_model_closed_forms():
+    m = bench.transfer_model(10 ** 9, {"cachegen": 2 * 10 ** 8, "int8": 5 * 10 ** 8},
+                             {"cachegen": 3.0, "int8": 1.0})
+    assert m["bandwidth_mbps"] == [100, 500, 1000]
+    # 1 GB = 8 Gbit: 80 s, 16 s, 8 s
+    assert m["raw_s"] == [80.0, 16.0, 8.0]
+    # 0.2 GB plus 3 ms of decode
+    assert m["cachegen_s"] == [16.003, 3.203, 1.603]
+    assert m["int8_s"] == [40.001, 8.001, 4.001]
+
+
+def test_rel_rmse():
+    x = torch.ones((2, 2, 3, 4), dtype=torch.bfloat16)
+    assert bench.rel_rmse(x, x) == 0.0
+    y = x * 1.5
+    assert abs(bench.rel_rmse(x, y) - 0.5) < 1e-12
+    assert bench.rel_rmse(torch.zeros_like(x), y) == 0.0

@@ -156,3 +156,22 @@ def test_container_open_reads_oracle_container(orc):
 def test_status_strings(lib):
     assert cg.cg_status_string(0) == "ok"
     assert "capacity" in cg.cg_status_string(cg.CG_ERR_CAPACITY)
+
+
+def test_int8_argument_checks(lib):
+    """Argument errors of the int8 baseline calls come back before any
+    device work is enqueued."""
+    P = ct.c_void_p
+    fake = P(4096)  # never dereferenced: every call below fails validation
+    assert lib.cg_int8_encode(fake, 4, 12, fake, fake, fake, None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_encode(fake, -1, 16, fake, fake, fake, None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_encode(fake, 4, 4104, fake, fake, fake, None) == cg.CG_ERR_UNSUPPORTED
+    assert lib.cg_int8_encode(fake, 4, 16, fake, fake, None, None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_encode(P(4098), 4, 16, fake, fake, fake, None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_encode(fake, 4, 16, P(4097), fake, fake, None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_encode(None, 4, 16, fake, fake, fake, None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_decode(fake, fake, 4, 0, fake, None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_decode(fake, fake, 4, 8192, fake, None) == cg.CG_ERR_UNSUPPORTED
+    assert lib.cg_int8_decode(fake, fake, 4, 16, P(4104), None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_decode(None, fake, 4, 16, fake, None) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_int8_decode(None, None, 0, 16, None, None) == cg.CG_OK

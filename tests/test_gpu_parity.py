@@ -109,6 +109,7 @@ EDGE = [
     (2, 64, 8, 512, 64, [(0, 2, 16)], [(0, 2, 16)], "normal"),      # C = 4096 (16 bins)
     (2, 100, 16, 128, 64, [(0, 2, 32)], [(0, 1, 16), (1, 2, 32)], "normal"),  # C = 2048
     (2, 256, 4, 64, 256, [(0, 2, 32)], [(0, 2, 16)], "bimodal"),    # near-half CDF splits
+    (2, 300, 2, 32, 256, [(0, 2, 64)], [(0, 2, 16)], "tiny"),       # amax near 2^-118
 ]
 
 
@@ -124,6 +125,9 @@ def _edge_bits(L, T, C, kind, seed):
         x = np.where(rng.random((L, 2, T, C)) < 0.5, -1.0, 1.0)
     elif kind == "constant":
         x = np.broadcast_to(rng.standard_normal((L, 2, T, 1)), (L, 2, T, C))
+    elif kind == "tiny":
+        # rows just above the smallest amax with a finite MAX / a
+        x = rng.standard_normal((L, 2, T, C)) * 2.0 ** -118
     elif kind == "extreme":
         x = rng.standard_normal((L, 2, T, C)) * np.exp(rng.uniform(-80, 80, (L, 2, T, 1)))
         x[..., 0] = 3.0e38
@@ -195,6 +199,23 @@ def test_nonfinite_input_is_reported():
     st, total = cg.cg_last_device_error(codec.plan, codec.workspace)
     assert st == cg.CG_ERR_NONFINITE
     assert 0 < total <= codec.sizes.max_stream_bytes
+
+
+def test_tiny_row_is_reported():
+    # a row whose amax (2^-126) makes MAX / a overflow fp32 has no scale factor
+    name = "opt125m_t256"
+    p = synthetic.WORKLOADS[name]
+    bits = synthetic.generate(name, num_tokens=64).copy()
+    bits[2, 0, 9, :] = 0
+    bits[2, 0, 9, 7] = 0x0080
+    k, v = synthetic.workload_specs(name)
+    L, _, T, C = bits.shape
+    codec = cg.Codec(L, T, p["H"], p["D"], 256, k, v)
+    enc = codec.alloc_encoded()
+    cg.cg_encode(codec.plan, _to_dev(bits, p["H"], p["D"]), codec.workspace, enc.bytestream,
+                 enc.lengths, enc.cdf, enc.amax)
+    st, _ = cg.cg_last_device_error(codec.plan, codec.workspace)
+    assert st == cg.CG_ERR_NONFINITE
 
 
 def test_capacity_too_small_is_reported_without_overrun(orc):

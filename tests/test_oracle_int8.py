@@ -113,3 +113,31 @@ def test_int8_whole_blob_matches_rows(orc):
         assert a == sc[r] and np.array_equal(qr, q.reshape(-1, C)[r])
     y = orc.int8_decode(q, sc)
     assert np.array_equal(y.reshape(-1, C)[5], orc.int8_dequant_row(q.reshape(-1, C)[5], sc[5]))
+
+
+def test_overflowing_scale_factor_rejected(orc):
+    """A row so small that MAX / a rounds to inf in fp32 has no scale
+    factor; both quantisers reject it (status 4, non-finite). The boundary
+    is where the exact quotient reaches 2^128 - 2^103, the point from which
+    round-to-nearest gives inf."""
+    limit = Fraction(2 ** 128 - 2 ** 103)
+    seen = {True: 0, False: 0}
+    for bits in list(range(1, 0x0400, 3)) + [0x0080, 0x0100, 0x0180]:
+        a = Fraction(_f(bits))
+        row = np.array([bits, 0, bits | 0x8000], np.uint16)
+        for M, call in ((127, lambda: orc.int8_quantize_row(row)),
+                        (7, lambda: orc.quantize_row(row, 16)),
+                        (15, lambda: orc.quantize_row(row, 32)),
+                        (31, lambda: orc.quantize_row(row, 64))):
+            overflow = Fraction(M) / a >= limit
+            seen[overflow] += 1
+            if overflow:
+                with pytest.raises(orc.OracleError) as e:
+                    call()
+                assert e.value.status == 4
+            else:
+                amax, q = call()
+                assert amax == float(a)
+                off = 0 if M == 127 else M
+                assert q.astype(int).tolist() == [off + M, off, off - M]
+    assert seen[True] > 20 and seen[False] > 20

@@ -35,8 +35,8 @@ MUTANTS = [
     ("dec-no-shift-in", "            value = 2 * value + get_bit(&br);", "            value = 2 * value;", "wnc or brute"),
     ("groups-255", "#define ORC_GROUP_TOKENS 256", "#define ORC_GROUP_TOKENS 255", "groups"),
     ("bins-allow-odd", "if (b < 4 || b > 64 || (b % 2) != 0)", "if (b < 4 || b > 64)", "layer_bins"),
-    ("int8-divide-form", "    float f = (a == 0.0f) ? 0.0f : 127.0f / a;\n    for (int32_t c = 0; c < C; ++c) {\n        float y = bf16_to_float(x[c]) * f;",
-     "    float f = (a == 0.0f) ? 0.0f : a / 127.0f;\n    for (int32_t c = 0; c < C; ++c) {\n        float y = (f == 0.0f) ? 0.0f : bf16_to_float(x[c]) / f;", "int8"),
+    ("int8-divide-form", "    float f = (a == 0.0f) ? 0.0f : 127.0f / a;\n    if (!isfinite(f)) /* as in orc_quantize_row */\n        return ORC_ERR_NONFINITE;\n    for (int32_t c = 0; c < C; ++c) {\n        float y = bf16_to_float(x[c]) * f;",
+     "    float f = (a == 0.0f) ? 0.0f : a / 127.0f;\n    if (!isfinite(f)) /* as in orc_quantize_row */\n        return ORC_ERR_NONFINITE;\n    for (int32_t c = 0; c < C; ++c) {\n        float y = (f == 0.0f) ? 0.0f : bf16_to_float(x[c]) / f;", "int8"),
     ("int8-scale-128", "float f = (a == 0.0f) ? 0.0f : 127.0f / a;", "float f = (a == 0.0f) ? 0.0f : 128.0f / a;", "int8"),
     ("int8-round-away", "        int32_t iq = (int32_t)rintf(y);\n        if (iq < -127", "        int32_t iq = (int32_t)roundf(y);\n        if (iq < -127", "int8"),
     ("int8-dequant-order", "        float t = (float)q[c] / 127.0f;\n        t = t * a;", "        float t = (float)q[c] * a;\n        t = t / 127.0f;", "int8"),
