@@ -123,6 +123,7 @@ typedef struct cg_sizes {
     int32_t num_tiles;        /* groups * 2 * L */
     int32_t encode_launches;  /* kernels one cg_encode enqueues */
     int32_t decode_launches;  /* kernels one cg_decode enqueues */
+    int32_t num_objects;      /* objects of chunk_tokens tokens (cg_object_range) */
 } cg_sizes;
 
 /* Device buffers of one encoded blob (all caller-owned). */
@@ -202,6 +203,54 @@ cg_status cg_container_open(const void *host_in, size_t len, cg_plan **plan_out,
  * Waits for stream before returning. */
 cg_status cg_deserialize(const cg_plan *plan, const void *host_in, size_t len,
                          const cg_encoded *dev_out, cg_stream_t stream);
+
+/* Objects. LMCache keeps a KV cache as objects of chunk_tokens tokens
+ * [CG-LMCache §4: chunk_size] (the last may be shorter). One cg_encode
+ * codes every object of a plan in the same launches; since token groups
+ * never span two objects, an object's CDF blocks, lengths and streams are
+ * exactly those of encoding its tokens alone. The calls below cut an
+ * encoded blob into one container per object, and put the containers of
+ * all objects back into device buffers for one cg_decode.
+ *
+ * cg_object_range: first token and token count of object (0 <= object <
+ * num_objects of cg_plan_sizes). Host only; CG_ERR_INVALID_ARG for an
+ * object out of range.
+ *
+ * cg_object_streams: after a cg_encode (or cg_decode) that used this
+ * workspace, the byte offset and length of the object's streams within the
+ * bytestream, read from the workspace. Waits for stream.
+ *
+ * cg_object_container_size: bytes of the object's container for
+ * stream_bytes bytes of streams. Host only.
+ *
+ * cg_serialize_object: write the object's container into host memory. It is
+ * the container format of cg_serialize for a plan with the same L, H, D,
+ * chunk_tokens and specs and T = the object's token count; its sections are
+ * the object's amax columns [2][L][n], lengths, CDF blocks and streams, so it
+ * is byte-identical to encoding and serialising the object's tokens alone.
+ * Waits for stream.
+ *
+ * cg_deserialize_objects: copy the containers of all num_objects objects,
+ * in object order (hosts[i] holds lens[i] bytes), into device buffers laid
+ * out as cg_encode writes them for the whole plan; *stream_bytes gets the
+ * total stream length to pass to cg_decode. Every header is checked before
+ * anything is copied: CG_ERR_CORRUPT if a container is not object i of this
+ * plan (shape, specs, tokens, groups, length), CG_ERR_CAPACITY if the
+ * streams do not fit, CG_ERR_INVALID_ARG if num_objects differs from the
+ * plan's. Waits for stream. */
+cg_status cg_object_range(const cg_plan *plan, int32_t object, int32_t *first_token,
+                          int32_t *num_tokens);
+cg_status cg_object_streams(const cg_plan *plan, const void *workspace, int32_t object,
+                            uint64_t *offset, uint64_t *bytes, cg_stream_t stream);
+cg_status cg_object_container_size(const cg_plan *plan, int32_t object, uint64_t stream_bytes,
+                                   size_t *bytes);
+cg_status cg_serialize_object(const cg_plan *plan, const cg_encoded *enc, const void *workspace,
+                              int32_t object, void *host_out, size_t host_capacity,
+                              size_t *written, cg_stream_t stream);
+cg_status cg_deserialize_objects(const cg_plan *plan, int32_t num_objects,
+                                 const void *const *hosts, const size_t *lens,
+                                 const cg_encoded *dev_out, uint64_t *stream_bytes,
+                                 cg_stream_t stream);
 
 /* Bytes of the fixed scratch array that cg_encode_noalloc uses (64 MiB). */
 #define CG_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)

@@ -39,7 +39,8 @@ class cg_sizes(ct.Structure):
                 ("cdf_entries", ct.c_size_t), ("num_streams", ct.c_size_t),
                 ("num_scales", ct.c_size_t), ("raw_bytes", ct.c_size_t),
                 ("num_groups", ct.c_int32), ("num_tiles", ct.c_int32),
-                ("encode_launches", ct.c_int32), ("decode_launches", ct.c_int32)]
+                ("encode_launches", ct.c_int32), ("decode_launches", ct.c_int32),
+                ("num_objects", ct.c_int32)]
 
 
 class cg_encoded(ct.Structure):
@@ -93,6 +94,15 @@ def load(build_if_missing: bool = True) -> ct.CDLL:
             "cg_deserialize": (st, [P, P, sz, ct.POINTER(cg_encoded), P]),
             "cg_status_string": (ct.c_char_p, [st]),
             "cg_encode_noalloc": (st, [P, P, ct.POINTER(cg_encoded), P, P]),
+            "cg_object_range": (st, [P, ct.c_int32, ct.POINTER(ct.c_int32),
+                                     ct.POINTER(ct.c_int32)]),
+            "cg_object_streams": (st, [P, P, ct.c_int32, ct.POINTER(u64), ct.POINTER(u64), P]),
+            "cg_object_container_size": (st, [P, ct.c_int32, u64, ct.POINTER(sz)]),
+            "cg_serialize_object": (st, [P, ct.POINTER(cg_encoded), P, ct.c_int32, P, sz,
+                                         ct.POINTER(sz), P]),
+            "cg_deserialize_objects": (st, [P, ct.c_int32, ct.POINTER(ct.c_void_p),
+                                            ct.POINTER(sz), ct.POINTER(cg_encoded),
+                                            ct.POINTER(u64), P]),
             "cg_int8_encode": (st, [P, ct.c_int64, ct.c_int32, P, P, P, P]),
             "cg_int8_decode": (st, [P, P, ct.c_int64, ct.c_int32, P, P]),
             "cg_profile_enable": (st, [P, ct.c_int32]),
@@ -207,6 +217,55 @@ def cg_int8_decode(q, scales, rows, channels, kv_out, stream=None) -> None:
     _check(load().cg_int8_decode(ct.c_void_p(_ptr(q)), ct.c_void_p(_ptr(scales)), int(rows),
                                  int(channels), ct.c_void_p(_ptr(kv_out)), _stream_handle(stream)),
            "cg_int8_decode")
+
+
+def cg_object_range(plan, obj):
+    """(first token, token count) of an object of the plan."""
+    t0, n = ct.c_int32(0), ct.c_int32(0)
+    _check(load().cg_object_range(ct.c_void_p(plan), int(obj), ct.byref(t0), ct.byref(n)),
+           "cg_object_range")
+    return t0.value, n.value
+
+
+def cg_object_streams(plan, workspace, obj, stream=None):
+    """(offset, bytes) of an object's streams in the last encoded bytestream."""
+    off, nb = ct.c_uint64(0), ct.c_uint64(0)
+    _check(load().cg_object_streams(ct.c_void_p(plan), ct.c_void_p(_ptr(workspace)), int(obj),
+                                    ct.byref(off), ct.byref(nb), _stream_handle(stream)),
+           "cg_object_streams")
+    return off.value, nb.value
+
+
+def cg_object_container_size(plan, obj, stream_bytes) -> int:
+    n = ct.c_size_t(0)
+    _check(load().cg_object_container_size(ct.c_void_p(plan), int(obj), int(stream_bytes),
+                                           ct.byref(n)), "cg_object_container_size")
+    return n.value
+
+
+def cg_serialize_object(plan, bytestream, lengths, cdf, amax, workspace, obj, host_out,
+                        stream=None) -> int:
+    enc = _encoded_struct(bytestream, lengths, cdf, amax)
+    w = ct.c_size_t(0)
+    _check(load().cg_serialize_object(ct.c_void_p(plan), ct.byref(enc),
+                                      ct.c_void_p(_ptr(workspace)), int(obj),
+                                      ct.c_void_p(host_out.data_ptr()), host_out.numel(),
+                                      ct.byref(w), _stream_handle(stream)), "cg_serialize_object")
+    return w.value
+
+
+def cg_deserialize_objects(plan, hosts, bytestream, lengths, cdf, amax, stream=None) -> int:
+    """hosts: uint8 CPU tensors, one container per object in object order.
+    Returns the total stream bytes."""
+    n = len(hosts)
+    ptrs = (ct.c_void_p * max(n, 1))(*[h.data_ptr() for h in hosts])
+    lens = (ct.c_size_t * max(n, 1))(*[h.numel() for h in hosts])
+    enc = _encoded_struct(bytestream, lengths, cdf, amax)
+    sb = ct.c_uint64(0)
+    _check(load().cg_deserialize_objects(ct.c_void_p(plan), n, ptrs, lens, ct.byref(enc),
+                                         ct.byref(sb), _stream_handle(stream)),
+           "cg_deserialize_objects")
+    return sb.value
 
 
 def int8_encode(kv, stream=None, sync: bool = True):
@@ -396,6 +455,27 @@ class Codec:
         w = cg_serialize(self.plan, enc.bytestream, enc.lengths, enc.cdf, enc.amax,
                          enc.stream_bytes, host_out, stream)
         return host_out[:w]
+
+    def object_bytes(self, enc: Encoded, stream=None):
+        """One container per object (uint8 CPU tensors) of the blob that the
+        last encode with this codec wrote into enc."""
+        import torch
+        out = []
+        for o in range(self.sizes.num_objects):
+            _, nb = cg_object_streams(self.plan, self.workspace, o, stream)
+            host = torch.empty(cg_object_container_size(self.plan, o, nb), dtype=torch.uint8,
+                               pin_memory=True)
+            w = cg_serialize_object(self.plan, enc.bytestream, enc.lengths, enc.cdf, enc.amax,
+                                    self.workspace, o, host, stream)
+            out.append(host[:w])
+        return out
+
+    def from_object_bytes(self, hosts, out: Encoded | None = None, stream=None) -> Encoded:
+        """Put the containers of all objects back for one decode."""
+        out = out or self.alloc_encoded()
+        out.stream_bytes = cg_deserialize_objects(self.plan, hosts, out.bytestream, out.lengths,
+                                                  out.cdf, out.amax, stream)
+        return out
 
     @staticmethod
     def from_bytes(host_in, device="cuda", stream=None):

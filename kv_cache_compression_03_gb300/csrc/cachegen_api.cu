@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -65,15 +66,71 @@ struct Sections {
     size_t amax, lengths, cdf, streams, end;
 };
 
-Sections sections(const cg_plan *p, uint64_t stream_bytes)
+// Section offsets of a container holding T tokens in ngroups groups.
+Sections sections_for(const cg_plan *p, int64_t T, int64_t ngroups, uint64_t stream_bytes)
 {
+    const size_t streams = (size_t)2 * p->L * (size_t)T;
     Sections s;
     s.amax = header_bytes(p);
-    s.lengths = s.amax + 4 * (size_t)p->num_streams;
-    s.cdf = s.lengths + 4 * (size_t)p->num_streams;
-    s.streams = s.cdf + 2 * (size_t)p->cdf_entries;
+    s.lengths = s.amax + 4 * streams;
+    s.cdf = s.lengths + 4 * streams;
+    s.streams = s.cdf + 2 * (size_t)p->tp.cdf_per_group * (size_t)ngroups;
     s.end = s.streams + (size_t)stream_bytes;
     return s;
+}
+
+Sections sections(const cg_plan *p, uint64_t stream_bytes)
+{
+    return sections_for(p, p->T, p->tp.ngroups, stream_bytes);
+}
+
+// Header and spec lists of a container of T tokens in ngroups groups.
+void write_header(uint8_t *h, const cg_plan *p, int32_t T, int32_t ngroups, uint64_t stream_bytes)
+{
+    put32(h + 0, kMagic);
+    put32(h + 4, kVersion);
+    put32(h + 8, (uint32_t)p->L);
+    put32(h + 12, (uint32_t)T);
+    put32(h + 16, (uint32_t)p->H);
+    put32(h + 20, (uint32_t)p->D);
+    put32(h + 24, (uint32_t)p->chunk_tokens);
+    put32(h + 28, (uint32_t)p->kspecs.size());
+    put32(h + 32, (uint32_t)p->vspecs.size());
+    put32(h + 36, (uint32_t)ngroups);
+    put32(h + 40, (uint32_t)(stream_bytes & 0xFFFFFFFFu));
+    put32(h + 44, (uint32_t)(stream_bytes >> 32));
+    uint8_t *q = h + kHeaderFixed;
+    for (const auto *list : {&p->kspecs, &p->vspecs})
+        for (const cg_quant_spec &s : *list) {
+            put32(q, (uint32_t)s.start_layer);
+            put32(q + 4, (uint32_t)s.end_layer);
+            put32(q + 8, (uint32_t)s.bins);
+            q += 12;
+        }
+}
+
+// Objects: runs of chunk_tokens tokens (the last may be shorter); groups
+// never span two objects, so object o owns groups [g0, g0 + ng).
+struct ObjectRange {
+    int32_t t0, n, g0, ng;
+};
+
+int32_t num_objects(const cg_plan *p)
+{
+    return p->tp.full_objects + ((int64_t)p->tp.full_objects * p->chunk_tokens < p->T ? 1 : 0);
+}
+
+bool object_range(const cg_plan *p, int32_t o, ObjectRange *r)
+{
+    if (o < 0 || o >= num_objects(p))
+        return false;
+    const int64_t t0 = (int64_t)o * p->chunk_tokens;
+    const int64_t n = std::min<int64_t>(p->chunk_tokens, p->T - t0);
+    r->t0 = (int32_t)t0;
+    r->n = (int32_t)n;
+    r->g0 = o * p->tp.groups_per_object;
+    r->ng = (int32_t)((n + CG_GROUP_TOKENS - 1) / CG_GROUP_TOKENS);
+    return true;
 }
 
 }  // namespace
@@ -291,6 +348,7 @@ cg_status cg_plan_sizes(const cg_plan *p, cg_sizes *out)
     out->num_tiles = p->tp.ntiles;
     out->encode_launches = cg_encode_launch_count(p);
     out->decode_launches = cg_decode_launch_count(p);
+    out->num_objects = num_objects(p);
     return CG_OK;
 }
 
@@ -374,31 +432,7 @@ cg_status cg_serialize(const cg_plan *p, const cg_encoded *enc, uint64_t stream_
     if (stream_bytes > enc->bytestream_capacity)
         return CG_ERR_CAPACITY;
     uint8_t *h = static_cast<uint8_t *>(host_out);
-    put32(h + 0, kMagic);
-    put32(h + 4, kVersion);
-    put32(h + 8, (uint32_t)p->L);
-    put32(h + 12, (uint32_t)p->T);
-    put32(h + 16, (uint32_t)p->H);
-    put32(h + 20, (uint32_t)p->D);
-    put32(h + 24, (uint32_t)p->chunk_tokens);
-    put32(h + 28, (uint32_t)p->kspecs.size());
-    put32(h + 32, (uint32_t)p->vspecs.size());
-    put32(h + 36, (uint32_t)p->tp.ngroups);
-    put32(h + 40, (uint32_t)(stream_bytes & 0xFFFFFFFFu));
-    put32(h + 44, (uint32_t)(stream_bytes >> 32));
-    uint8_t *q = h + kHeaderFixed;
-    for (const cg_quant_spec &s : p->kspecs) {
-        put32(q, (uint32_t)s.start_layer);
-        put32(q + 4, (uint32_t)s.end_layer);
-        put32(q + 8, (uint32_t)s.bins);
-        q += 12;
-    }
-    for (const cg_quant_spec &s : p->vspecs) {
-        put32(q, (uint32_t)s.start_layer);
-        put32(q + 4, (uint32_t)s.end_layer);
-        put32(q + 8, (uint32_t)s.bins);
-        q += 12;
-    }
+    write_header(h, p, p->T, p->tp.ngroups, stream_bytes);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(h + sec.amax, enc->amax, 4 * (size_t)p->num_streams,
                                     cudaMemcpyDeviceToHost, s);
@@ -498,4 +532,160 @@ cg_status cg_deserialize(const cg_plan *p, const void *host_in, size_t len,
     return e == cudaSuccess ? CG_OK : CG_ERR_CUDA;
 }
 
+cg_status cg_object_range(const cg_plan *p, int32_t object, int32_t *first_token,
+                          int32_t *num_tokens)
+{
+    ObjectRange r;
+    if (p == nullptr || !object_range(p, object, &r))
+        return CG_ERR_INVALID_ARG;
+    if (first_token)
+        *first_token = r.t0;
+    if (num_tokens)
+        *num_tokens = r.n;
+    return CG_OK;
+}
+
+cg_status cg_object_streams(const cg_plan *p, const void *workspace, int32_t object,
+                            uint64_t *offset, uint64_t *bytes, cg_stream_t stream)
+{
+    ObjectRange r;
+    if (p == nullptr || workspace == nullptr || !object_range(p, object, &r))
+        return CG_ERR_INVALID_ARG;
+    // tile bases are ordered group, K/V, layer and end with the total
+    const uint64_t *base = reinterpret_cast<const uint64_t *>(
+        static_cast<const uint8_t *>(workspace) + p->ws_tile_base);
+    const size_t first = (size_t)r.g0 * 2 * p->L, last = (size_t)(r.g0 + r.ng) * 2 * p->L;
+    uint64_t b0 = 0, b1 = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&b0, base + first, 8, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&b1, base + last, 8, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return CG_ERR_CUDA;
+    if (b1 < b0)
+        return CG_ERR_CORRUPT;
+    if (offset)
+        *offset = b0;
+    if (bytes)
+        *bytes = b1 - b0;
+    return CG_OK;
+}
+
+cg_status cg_object_container_size(const cg_plan *p, int32_t object, uint64_t stream_bytes,
+                                   size_t *bytes)
+{
+    ObjectRange r;
+    if (p == nullptr || bytes == nullptr || !object_range(p, object, &r))
+        return CG_ERR_INVALID_ARG;
+    *bytes = sections_for(p, r.n, r.ng, stream_bytes).end;
+    return CG_OK;
+}
+
+cg_status cg_serialize_object(const cg_plan *p, const cg_encoded *enc, const void *workspace,
+                              int32_t object, void *host_out, size_t host_capacity,
+                              size_t *written, cg_stream_t stream)
+{
+    ObjectRange r;
+    if (p == nullptr || enc == nullptr || host_out == nullptr || !object_range(p, object, &r))
+        return CG_ERR_INVALID_ARG;
+    uint64_t off = 0, sb = 0;
+    cg_status st = cg_object_streams(p, workspace, object, &off, &sb, stream);
+    if (st != CG_OK)
+        return st;
+    const Sections sec = sections_for(p, r.n, r.ng, sb);
+    if (host_capacity < sec.end)
+        return CG_ERR_CAPACITY;
+    if (off + sb > enc->bytestream_capacity)
+        return CG_ERR_CAPACITY;
+    uint8_t *h = static_cast<uint8_t *>(host_out);
+    write_header(h, p, r.n, r.ng, sb);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // amax [2][L][T] -> the object's columns, as [2][L][n]
+    cudaError_t e = cudaMemcpy2DAsync(h + sec.amax, 4 * (size_t)r.n, enc->amax + r.t0,
+                                      4 * (size_t)p->T, 4 * (size_t)r.n, (size_t)2 * p->L,
+                                      cudaMemcpyDeviceToHost, s);
+    // its streams (and their lengths) and CDF blocks are contiguous
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h + sec.lengths, enc->lengths + (size_t)2 * p->L * r.t0,
+                            (size_t)8 * p->L * r.n, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h + sec.cdf, enc->cdf + (size_t)r.g0 * p->tp.cdf_per_group,
+                            sec.streams - sec.cdf, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && sb > 0)
+        e = cudaMemcpyAsync(h + sec.streams, enc->bytestream + off, (size_t)sb,
+                            cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return CG_ERR_CUDA;
+    if (written)
+        *written = sec.end;
+    return CG_OK;
+}
+
+cg_status cg_deserialize_objects(const cg_plan *p, int32_t n, const void *const *hosts,
+                                 const size_t *lens, const cg_encoded *dev,
+                                 uint64_t *stream_bytes, cg_stream_t stream)
+{
+    if (p == nullptr || hosts == nullptr || lens == nullptr || dev == nullptr)
+        return CG_ERR_INVALID_ARG;
+    if (!dev->bytestream || !dev->lengths || !dev->cdf || !dev->amax)
+        return CG_ERR_INVALID_ARG;
+    if (n != num_objects(p))
+        return CG_ERR_INVALID_ARG;
+    // check every header before copying anything
+    const size_t hb = header_bytes(p);
+    std::vector<uint8_t> want(hb);
+    std::vector<uint64_t> sbs(n);
+    uint64_t total = 0;
+    for (int32_t o = 0; o < n; ++o) {
+        ObjectRange r;
+        object_range(p, o, &r);
+        const uint8_t *h = static_cast<const uint8_t *>(hosts[o]);
+        if (h == nullptr)
+            return CG_ERR_INVALID_ARG;
+        if (lens[o] < hb)
+            return CG_ERR_CORRUPT;
+        const uint64_t sb = (uint64_t)get32(h + 40) | ((uint64_t)get32(h + 44) << 32);
+        write_header(want.data(), p, r.n, r.ng, sb);
+        if (memcmp(want.data(), h, hb) != 0 || sections_for(p, r.n, r.ng, sb).end != lens[o])
+            return CG_ERR_CORRUPT;
+        sbs[o] = sb;
+        total += sb;
+    }
+    if (dev->bytestream_capacity < align_up((size_t)total, 16))
+        return CG_ERR_CAPACITY;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    uint64_t off = 0;
+    for (int32_t o = 0; o < n && e == cudaSuccess; ++o) {
+        ObjectRange r;
+        object_range(p, o, &r);
+        const uint8_t *h = static_cast<const uint8_t *>(hosts[o]);
+        const Sections sec = sections_for(p, r.n, r.ng, sbs[o]);
+        e = cudaMemcpy2DAsync(dev->amax + r.t0, 4 * (size_t)p->T, h + sec.amax, 4 * (size_t)r.n,
+                              4 * (size_t)r.n, (size_t)2 * p->L, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dev->lengths + (size_t)2 * p->L * r.t0, h + sec.lengths,
+                                (size_t)8 * p->L * r.n, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dev->cdf + (size_t)r.g0 * p->tp.cdf_per_group, h + sec.cdf,
+                                sec.streams - sec.cdf, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess && sbs[o] > 0)
+            e = cudaMemcpyAsync(dev->bytestream + off, h + sec.streams, (size_t)sbs[o],
+                                cudaMemcpyHostToDevice, s);
+        off += sbs[o];
+    }
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return CG_ERR_CUDA;
+    if (stream_bytes)
+        *stream_bytes = total;
+    return CG_OK;
+}
+
 }  // extern "C"
+

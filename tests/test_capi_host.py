@@ -3,6 +3,7 @@ exports every function include/cachegen.h declares, configuration
 validation matches the oracle's, sizes follow the layout, and a container
 written by the oracle opens with the same plan."""
 import ctypes as ct
+import struct
 import os
 import re
 import subprocess
@@ -175,3 +176,91 @@ def test_int8_argument_checks(lib):
     assert lib.cg_int8_decode(fake, fake, 4, 16, P(4104), None) == cg.CG_ERR_INVALID_ARG
     assert lib.cg_int8_decode(None, fake, 4, 16, fake, None) == cg.CG_ERR_INVALID_ARG
     assert lib.cg_int8_decode(None, None, 0, 16, None, None) == cg.CG_OK
+
+
+def _object_containers(orc, name, T, ch):
+    p = synthetic.WORKLOADS[name]
+    kv = synthetic.generate(name, num_tokens=T)
+    k, v = synthetic.workload_specs(name)
+    L, C = kv.shape[0], kv.shape[-1]
+    blobs = []
+    for t0 in range(0, T, ch):
+        part = np.ascontiguousarray(kv[:, :, t0:t0 + ch])
+        enc = orc.encode(part, ch, k, v)
+        blobs.append(orc.serialize(enc, L, part.shape[2], p["H"], p["D"], ch, k, v))
+    return p, k, v, L, blobs
+
+
+def test_object_ranges_and_sizes(orc):
+    import torch
+    name = "opt125m_t256"
+    T, ch = 600, 128
+    p, k, v, L, blobs = _object_containers(orc, name, T, ch)
+    plan = cg.cg_plan_create(L, T, p["H"], p["D"], ch, k, v)
+    try:
+        s = cg.cg_plan_sizes(plan)
+        assert s.num_objects == 5 == len(blobs)
+        for o, blob in enumerate(blobs):
+            t0, n = cg.cg_object_range(plan, o)
+            assert (t0, n) == (o * ch, min(ch, T - o * ch))
+            # the size rule agrees with the oracle's container of the slice
+            sb = struct.unpack_from("<Q", blob, 40)[0]
+            assert cg.cg_object_container_size(plan, o, sb) == len(blob)
+            # and the slice's own plan opens it
+            oplan, osb = cg.cg_container_open(torch.from_numpy(np.frombuffer(blob, np.uint8).copy()))
+            cg.cg_plan_destroy(oplan)
+            assert osb == sb
+        for bad in (-1, 5):
+            with pytest.raises(cg.CacheGenError):
+                cg.cg_object_range(plan, bad)
+    finally:
+        cg.cg_plan_destroy(plan)
+
+
+def test_deserialize_objects_checks_headers_first(orc, lib):
+    """Containers that are not object i of the plan are rejected before any
+    copy (no device is touched here)."""
+    import torch
+    name = "opt125m_t256"
+    T, ch = 600, 256
+    p, k, v, L, blobs = _object_containers(orc, name, T, ch)
+    plan = cg.cg_plan_create(L, T, p["H"], p["D"], ch, k, v)
+    fake = torch.zeros(64, dtype=torch.uint8)  # never written: validation fails first
+    hosts = [torch.from_numpy(np.frombuffer(b, np.uint8).copy()) for b in blobs]
+    try:
+        def call(hs, pl=plan):
+            # the C call itself, on the default stream (the binding would ask
+            # torch for the current CUDA stream)
+            n = len(hs)
+            ptrs = (ct.c_void_p * n)(*[h.data_ptr() for h in hs])
+            lens = (ct.c_size_t * n)(*[h.numel() for h in hs])
+            enc = cg.cg_encoded(fake.data_ptr(), 64, fake.data_ptr(), fake.data_ptr(),
+                                fake.data_ptr())
+            sb = ct.c_uint64(0)
+            st = lib.cg_deserialize_objects(ct.c_void_p(pl), n, ptrs, lens, ct.byref(enc),
+                                            ct.byref(sb), None)
+            if st != cg.CG_OK:
+                raise cg.CacheGenError(st, "cg_deserialize_objects")
+        with pytest.raises(cg.CacheGenError) as e:
+            call(hosts[:2])                                  # wrong object count
+        assert e.value.status == cg.CG_ERR_INVALID_ARG
+        with pytest.raises(cg.CacheGenError) as e:
+            call([hosts[2], hosts[1], hosts[0]])             # the short tail first
+        assert e.value.status == cg.CG_ERR_CORRUPT
+        with pytest.raises(cg.CacheGenError) as e:
+            call([hosts[0], hosts[1], hosts[2][:-1]])        # truncated
+        assert e.value.status == cg.CG_ERR_CORRUPT
+        bad = hosts[1].clone()
+        bad[12] += 1                                         # token count
+        with pytest.raises(cg.CacheGenError) as e:
+            call([hosts[0], bad, hosts[2]])
+        assert e.value.status == cg.CG_ERR_CORRUPT
+        plan2 = cg.cg_plan_create(L, T, p["H"], p["D"], ch, [(0, 12, 16)], v)  # other specs
+        try:
+            with pytest.raises(cg.CacheGenError) as e:
+                call(hosts, plan2)
+            assert e.value.status == cg.CG_ERR_CORRUPT
+        finally:
+            cg.cg_plan_destroy(plan2)
+    finally:
+        cg.cg_plan_destroy(plan)

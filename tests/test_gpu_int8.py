@@ -49,7 +49,7 @@ def test_int8_parity_workloads(orc, name, T):
 @pytest.mark.parametrize("C", [8, 16, 248, 264, 768, 1032, 2056, 4096])
 def test_int8_ragged_row_lengths(orc, C):
     rng = np.random.default_rng(C)
-    x = rng.standard_normal((37, C)).astype(np.float32) * rng.lognormal(0, 2, (37, 1))
+    x = (rng.standard_normal((37, C)) * rng.lognormal(0, 2, (37, 1))).astype(np.float32)
     u = x.view(np.uint32)
     bits = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
     bits[3] = 0          # all-zero row
