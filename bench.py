@@ -309,6 +309,83 @@ def measure_baselines(cg, kv, cg_out, raw, container, t_dec_ms, peak, stream, de
     }
 
 
+def sweep_settings(L: int):
+    """Bin settings of the sweep: the preset, then every layer at 8, 16, 32
+    and 64 bins, then the preset with its 32-bin ranges widened (K's first
+    L/2 layers, V's first 10)."""
+    from kv_cache_compression_03_gb300 import cachegen as cg
+    k, v = cg.preset_specs(L)
+    out = [("preset", k, v)]
+    for b in (8, 16, 32, 64):
+        out.append((f"uniform{b}", [(0, L, b)], [(0, L, b)]))
+    if L >= 20:
+        out.append(("preset_wide32", [(0, L // 2, 32), (L // 2, L, 16)],
+                    [(0, 10, 32), (10, L, 16)]))
+    return out
+
+
+def run_bins_sweep(args):
+    """Compression ratio against reconstruction error for several bin
+    settings on one workload: one JSON line per setting (device-timed
+    encode and decode over --steps steps)."""
+    import numpy as np
+    import torch
+
+    from kv_cache_compression_03_gb300 import cachegen as cg
+    from kv_cache_compression_03_gb300 import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    name = args.workload
+    p, _, _ = workload_info(name)
+    L, T, H, D = p["L"], (args.tokens or p["T"]), p["H"], p["D"]
+    ch = p["chunk_tokens"][0]
+    bits = synthetic.generate(name, num_tokens=T)
+    kv = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(L, 2, T, H, D).to(dev)
+    del bits
+    stream = torch.cuda.current_stream(dev)
+    for label, k, v in sweep_settings(L):
+        try:
+            codec = cg.Codec(L, T, H, D, ch, k, v, device=dev)
+        except cg.CacheGenError as e:
+            print(json.dumps({"sweep": "bins", "workload": name, "setting": label,
+                              "unavailable": str(e)}), flush=True)
+            continue
+        enc = codec.encode(kv)
+        out = codec.decode(enc)
+        raw = codec.sizes.raw_bytes
+        container = cg.cg_container_size(codec.plan, enc.stream_bytes)
+        for _ in range(args.warmup):
+            codec.encode(kv, enc, sync=False, stream=stream)
+            codec.decode(enc, out, sync=False, stream=stream)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for _ in range(args.steps):
+            codec.encode(kv, enc, sync=False, stream=stream)
+        ev[1].record(stream)
+        for _ in range(args.steps):
+            codec.decode(enc, out, sync=False, stream=stream)
+        ev[2].record(stream)
+        torch.cuda.synchronize(dev)
+        st, _ = cg.cg_last_device_error(codec.plan, codec.workspace)
+        assert st == cg.CG_OK, st
+        t_e = ev[0].elapsed_time(ev[1]) / args.steps
+        t_d = ev[1].elapsed_time(ev[2]) / args.steps
+        line = {"sweep": "bins", "workload": name, "tokens": T, "setting": label,
+                "kspecs": [list(s) for s in k], "vspecs": [list(s) for s in v],
+                "compression_ratio": round(raw / container, 4),
+                "stream_bits_per_value": round(8 * enc.stream_bytes / (raw / 2), 4),
+                "rel_rmse": round(rel_rmse(kv, out), 6),
+                "rel_rmse_k": round(rel_rmse(kv[:, 0:1], out[:, 0:1]), 6),
+                "rel_rmse_v": round(rel_rmse(kv[:, 1:2], out[:, 1:2]), 6),
+                "encode_gbs": round(raw / (t_e * 1e-3) / 1e9, 2),
+                "decode_gbs": round(raw / (t_d * 1e-3) / 1e9, 2)}
+        print(json.dumps(line), flush=True)
+        del codec, enc, out
+    return 0
+
+
 def run_codec(args):
     import numpy as np
     import torch
@@ -498,9 +575,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the int8/naive comparison codecs and the transfer-time model")
+    ap.add_argument("--sweep-bins", action="store_true",
+                    help="instead of the benchmark line: ratio vs reconstruction error for "
+                         "several bin settings, one JSON line each")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.sweep_bins:
+        return run_bins_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_codec(args)

@@ -27,3 +27,14 @@ def test_rel_rmse():
     y = x * 1.5
     assert abs(bench.rel_rmse(x, y) - 0.5) < 1e-12
     assert bench.rel_rmse(torch.zeros_like(x), y) == 0.0
+
+
+def test_sweep_settings_are_valid_spec_lists(orc):
+    for L in (6, 12, 32, 40):
+        seen = set()
+        for label, k, v in bench.sweep_settings(L):
+            assert label not in seen
+            seen.add(label)
+            orc.layer_bins(L, k)   # raises on lists that do not tile [0, L)
+            orc.layer_bins(L, v)
+        assert "preset" in seen and "uniform16" in seen
