@@ -218,7 +218,9 @@ __device__ __forceinline__ void enc_store_if_full(Enc &e)
 {
     if (e.nb >= 32) {
         e.nb -= 32;
-        const uint32_t ov = e.a1 >> e.nb;
+        // nb < 32 here except in a batch that overfilled the buffer (then
+        // flagged); the clamping shifts keep that case defined
+        const uint32_t ov = __funnelshift_rc(e.a1, 0u, e.nb);  // a1 >> nb
         const uint32_t w = __funnelshift_r(e.a0, e.a1, e.nb);
         if (EXACT) {
             if (ov != 0)
@@ -235,7 +237,7 @@ __device__ __forceinline__ void enc_store_if_full(Enc &e)
         }
         e.wp++;
         e.a1 = 0;
-        e.a0 &= (1u << e.nb) - 1u;  // nb < 32 here
+        e.a0 &= ~__funnelshift_lc(0u, 0xFFFFFFFFu, e.nb);  // the low nb bits
     }
 }
 
@@ -252,9 +254,19 @@ __device__ __forceinline__ uint32_t add_with_carry(uint32_t x, uint32_t t, uint3
     return xs;
 }
 
+// Symbols per store check in the fast path. A symbol the encoder codes
+// occurs in its group, so its frequency is >= 256 of 2^16 and it adds at most
+// 9 bits (1.6 on average here). Fewer than 32 bits are left after a check, so
+// a batch overfills the 64-bit buffer (60 bits plus room for the batch's
+// carries above them) only if its symbols are nearly all among their groups'
+// rarest. The check flags that case and the stream is coded again on the
+// exact path, which checks after every symbol.
+constexpr int kStoreEvery = 4;
+
 // One symbol with CDF bounds c0 < c1 (c1 in 1..65535: the encoder never
-// codes the top symbol, whose upper bound would be 65536).
-template <bool EXACT>
+// codes the top symbol, whose upper bound would be 65536). STORE: take a
+// completed word out of the buffer afterwards.
+template <bool EXACT, bool STORE = true>
 __device__ __forceinline__ void enc_symbol(Enc &e, uint32_t c0, uint32_t c1)
 {
     const uint32_t t0 = scale16(e.d, c0);
@@ -270,7 +282,11 @@ __device__ __forceinline__ void enc_symbol(Enc &e, uint32_t c0, uint32_t c1)
     e.x = xs << S;
     e.d = __funnelshift_l(0xFFFFFFFFu, dn, S);
     e.nb += S;
-    enc_store_if_full<EXACT>(e);
+    if (STORE) {
+        if (!EXACT && kStoreEvery > 1)
+            e.flag |= (e.nb > 60u) ? 1u : 0u;
+        enc_store_if_full<EXACT>(e);
+    }
 }
 
 // Termination: the code value is the frame start plus 1/4 of the window
@@ -299,7 +315,7 @@ __device__ __forceinline__ uint32_t enc_finish(Enc &e)
         e.out[(int32_t)min(e.wp, e.cap) - 1] = __byte_perm(prev, 0, 0x0123);
     }
     if (e.nb) {
-        const uint32_t w = e.a0 << (32u - e.nb);
+        const uint32_t w = __funnelshift_lc(0u, e.a0, 32u - e.nb);  // a0 << (32 - nb)
         if (e.wp < e.cap)
             e.out[e.wp] = __byte_perm(w, 0, 0x0123);
         e.wp++;
@@ -340,7 +356,10 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
                 const uint32_t s = __byte_perm(word, 0, 0x4440 + (j & 3));
                 // s <= 2*MAX = N - 2, so cdf[s + 1] is never the top entry
                 // (65536, stored as 0)
-                enc_symbol<EXACT>(e, trow[s], trow[s + 1]);
+                if (EXACT || (j % kStoreEvery) == kStoreEvery - 1)
+                    enc_symbol<EXACT, true>(e, trow[s], trow[s + 1]);
+                else
+                    enc_symbol<EXACT, false>(e, trow[s], trow[s + 1]);
                 trow += Lp;
             }
         }
@@ -354,7 +373,10 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t s = __byte_perm(j < 4 ? v.x : v.y, 0, 0x4440 + (j & 3));
-                enc_symbol<EXACT>(e, trow[s], trow[s + 1]);
+                if (EXACT || (j % kStoreEvery) == kStoreEvery - 1)
+                    enc_symbol<EXACT, true>(e, trow[s], trow[s + 1]);
+                else
+                    enc_symbol<EXACT, false>(e, trow[s], trow[s + 1]);
                 trow += Lp;
             }
         }
@@ -799,6 +821,125 @@ __device__ __forceinline__ void bits_skip(Bits &r, uint32_t S)
     bits_refill(r);
 }
 
+// Refill for the batched loop below: avail may have gone negative there (a
+// batch needed more bits than were buffered; that stream is decoded again),
+// so both shifts clamp.
+__device__ __forceinline__ void bits_refill_clamped(Bits &r)
+{
+    if (r.avail <= 32) {
+        const uint32_t w = bits_word(r);
+        r.b1 |= __funnelshift_rc(w, 0u, (uint32_t)r.avail);        // w >> avail
+        r.b0 = __funnelshift_lc(0u, w, (uint32_t)(32 - r.avail));  // w << (32 - avail)
+        r.pos += 4;
+        r.avail += 32;
+    }
+}
+
+// Symbols per bit-buffer refill in the decoder's main loop. After a refill
+// the buffer holds at least 32 bits. A symbol that occurs in its group has
+// frequency >= (65536 - N) / 256 of 2^16, so it takes at most 10 bits, and
+// four of them fit unless all four are among the group's rarest; a batch that
+// does run short is detected (the count of buffered bits goes negative) and
+// the stream is decoded again refilling after every symbol.
+constexpr int kRefillEvery = 4;
+
+// Decode one stream (C symbols with the CDF rows of `table`) and write its
+// dequantised row. R > 1 refills the bit buffer once per R symbols and
+// returns 1 when a batch ran short of bits (the output is then wrong and the
+// caller decodes the stream again with R = 1, which never runs short: a
+// symbol takes at most 18 bits and the buffer holds at least 33 after every
+// refill).
+template <int NB, int R>
+__device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t C, int32_t N,
+                                                  Bits br, float a, const float *deq,
+                                                  uint16_t *orow)
+{
+    const int32_t Lp = N + 1;
+    // state: x = window of the absolute low end, d = range - 1,
+    // v = code value - low end
+    uint32_t x = 0, d = 0xFFFFFFFFu;
+    uint32_t v = br.b1;
+    bits_skip(br, 16);
+    bits_skip(br, 16);
+    const uint16_t *row = table;
+    const uint32_t top_step = 1u << (31 - __clz((uint32_t)(N - 1)));
+    uint32_t short_batch = 0;
+
+    for (int32_t c0 = 0; c0 < C; c0 += 8) {
+        uint32_t packed[4];
+        float y_even = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's
+            // own comparison, so the result is exact)
+            uint32_t s = 0;
+            if (NB > 0 && (NB & (NB - 1)) == 0) {
+#pragma unroll
+                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
+                    if (scale16(d, row[s + step]) <= v)
+                        s += step;
+            } else {
+                for (uint32_t step = top_step; step != 0; step >>= 1) {
+                    const uint32_t t = s + step;
+                    if (t < (uint32_t)N && scale16(d, row[t]) <= v)
+                        s = t;
+                }
+            }
+            const uint32_t c0v = row[s];
+            const uint32_t c1r = row[s + 1];  // 0 stands for 65536
+            const uint32_t t0 = scale16(d, c0v);
+            const uint32_t t1 = (c1r == 0) ? d + 1u : scale16(d, c1r);
+            const uint32_t dn = t1 - t0 - 1u;
+            // renormalise (see Enc); v takes S new bits
+            const uint32_t xs = x + t0;
+            const uint32_t hs = xs + dn;
+            const uint32_t n = __clz(xs ^ hs);
+            const uint32_t k = __clz((~xs | hs) << (n + 1u));
+            const uint32_t S = n + k;
+            x = xs << S;
+            d = __funnelshift_l(0xFFFFFFFFu, dn, S);
+            v = __funnelshift_l(br.b1, v - t0, S);
+            if (R == 1) {
+                bits_skip(br, S);
+            } else {
+                br.b1 = __funnelshift_l(br.b0, br.b1, S);
+                br.b0 <<= S;
+                br.avail -= (int32_t)S;
+                if ((j % R) == R - 1) {
+                    short_batch |= (br.avail < 0) ? 1u : 0u;
+                    bits_refill_clamped(br);
+                }
+            }
+            // dequantise: bf16(fp32((q - MAX) / MAX) * a), two values per
+            // conversion (each rounded to nearest even on its own)
+            const float y = __fmul_rn(deq[s], a);
+            if (j & 1) {
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(y_even, y);
+                packed[j >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
+            } else {
+                y_even = y;
+            }
+            row += Lp;
+        }
+        *reinterpret_cast<uint4 *>(orow + c0) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+    return short_batch;
+}
+
+// The refill-per-symbol decode of one stream, out of line: it runs only for
+// streams whose batched decode ran short of bits.
+template <int NB>
+__device__ __noinline__ void decode_stream_exact(const uint16_t *table, int32_t C, int32_t N,
+                                                 const uint8_t *bytestream, uint64_t sb,
+                                                 uint64_t last, float a, const float *deq,
+                                                 uint16_t *orow)
+{
+    Bits br;
+    bits_init(br, bytestream, sb, last);
+    decode_stream<NB, 1>(table, C, N, br, a, deq, orow);
+}
+
 // One tile of the decoder; NB as in encode_tile.
 template <int NB>
 __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params &P,
@@ -862,67 +1003,12 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
         set_status(status, CG_ERR_CORRUPT);
         sb = min(sb, last);
     }
-    Bits br;
-    bits_init(br, bytestream, sb, last);
-    // state: x = window of the absolute low end, d = range - 1,
-    // v = code value - low end
-    uint32_t x = 0, d = 0xFFFFFFFFu;
-    uint32_t v = br.b1;
-    bits_skip(br, 16);
-    bits_skip(br, 16);
     const float a = amax[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + tid];
     uint16_t *orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + tid) * (size_t)C;
-    const uint16_t *row = table;
-    const uint32_t top_step = 1u << (31 - __clz((uint32_t)(N - 1)));
-
-    for (int32_t c0 = 0; c0 < C; c0 += 8) {
-        uint32_t packed[4];
-        float y_even = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's
-            // own comparison, so the result is exact)
-            uint32_t s = 0;
-            if (NB > 0 && (NB & (NB - 1)) == 0) {
-#pragma unroll
-                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
-                    if (scale16(d, row[s + step]) <= v)
-                        s += step;
-            } else {
-                for (uint32_t step = top_step; step != 0; step >>= 1) {
-                    const uint32_t t = s + step;
-                    if (t < (uint32_t)N && scale16(d, row[t]) <= v)
-                        s = t;
-                }
-            }
-            const uint32_t c0v = row[s];
-            const uint32_t c1v = (((uint32_t)row[s + 1] + 0xFFFFu) & 0xFFFFu) + 1u;  // 0 -> 65536
-            const uint32_t t0 = scale16(d, c0v);
-            const uint32_t dn = scale16(d, c1v) - t0 - 1u;
-            // renormalise (see Enc); v takes S new bits
-            const uint32_t xs = x + t0;
-            const uint32_t hs = xs + dn;
-            const uint32_t n = __clz(xs ^ hs);
-            const uint32_t k = __clz((~xs | hs) << (n + 1u));
-            const uint32_t S = n + k;
-            x = xs << S;
-            d = __funnelshift_l(0xFFFFFFFFu, dn, S);
-            v = __funnelshift_l(br.b1, v - t0, S);
-            bits_skip(br, S);
-            // dequantise: bf16(fp32((q - MAX) / MAX) * a), two values per
-            // conversion (each rounded to nearest even on its own)
-            const float y = __fmul_rn(deq[s], a);
-            if (j & 1) {
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(y_even, y);
-                packed[j >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
-            } else {
-                y_even = y;
-            }
-            row += Lp;
-        }
-        *reinterpret_cast<uint4 *>(orow + c0) =
-            make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    }
+    Bits br;
+    bits_init(br, bytestream, sb, last);
+    if (decode_stream<NB, kRefillEvery>(table, C, N, br, a, deq, orow))
+        decode_stream_exact<NB>(table, C, N, bytestream, sb, last, a, deq, orow);
 }
 
 // Decoder tiles of one launch class (NB bins; 0 = any), at least MINB
@@ -964,7 +1050,7 @@ encode_fn encode_kernel(int32_t bins)
 decode_fn decode_kernel(int32_t bins)
 {
     if (bins == 16)
-        return k_decode_class<16, 5>;
+        return k_decode_class<16, 6>;
     if (bins == 32)
         return k_decode_class<32, 3>;
     return k_decode_class<0, 3>;

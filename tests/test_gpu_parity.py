@@ -110,6 +110,8 @@ EDGE = [
     (2, 100, 16, 128, 64, [(0, 2, 32)], [(0, 1, 16), (1, 2, 32)], "normal"),  # C = 2048
     (2, 256, 4, 64, 256, [(0, 2, 32)], [(0, 2, 16)], "bimodal"),    # near-half CDF splits
     (2, 300, 2, 32, 256, [(0, 2, 64)], [(0, 2, 16)], "tiny"),       # amax near 2^-118
+    (2, 512, 2, 64, 256, [(0, 2, 16)], [(0, 2, 32)], "sparse"),     # rows of rare symbols only
+    (1, 256, 1, 64, 256, [(0, 1, 16)], [(0, 1, 16)], "sparse1"),    # one busy row per group
 ]
 
 
@@ -125,6 +127,16 @@ def _edge_bits(L, T, C, kind, seed):
         x = np.where(rng.random((L, 2, T, C)) < 0.5, -1.0, 1.0)
     elif kind == "constant":
         x = np.broadcast_to(rng.standard_normal((L, 2, T, 1)), (L, 2, T, C))
+    elif kind in ("sparse", "sparse1"):
+        # most token rows are zero (every symbol is MAX); a few rows hold
+        # values, so each of their symbols occurs once or twice in its
+        # channel's group: ~8-9 bits per symbol, which fills the coders' bit
+        # buffers between checks
+        x = np.zeros((L, 2, T, C))
+        busy = [37] if kind == "sparse1" else [3, 100, 101, 255, 300, 511]
+        for t in busy:
+            if t < T:
+                x[:, :, t, :] = rng.standard_normal((L, 2, C))
     elif kind == "tiny":
         # rows just above the smallest amax with a finite MAX / a
         x = rng.standard_normal((L, 2, T, C)) * 2.0 ** -118
@@ -271,3 +283,45 @@ def test_corrupt_containers_are_reported(orc):
     e4.lengths[9] = -5
     assert decode_status(e4)[0] == cg.CG_ERR_CORRUPT
     assert decode_status(base, sb=base.stream_bytes - 16)[0] == cg.CG_ERR_CORRUPT
+
+
+def test_decoder_batches_that_run_short(orc):
+    """The decoder refills its bit buffer once per few symbols; a run of
+    symbols of frequency 1/65536 (which this encoder never produces, but a
+    valid container may hold) takes ~16 bits each, so such a batch runs short
+    and the stream is decoded again exactly. Built by hand: CDF rows with two
+    frequency-1 symbols, streams coded by the oracle's coder."""
+    L, T, H, D, N = 1, 64, 1, 32, 16
+    C = H * D
+    rng = np.random.default_rng(77)
+    row = np.zeros(N + 1, dtype=np.int64)
+    row[1], row[2] = 1, 2
+    row[2:] = 2 + np.round(np.arange(N - 1) * (65534 / (N - 2))).astype(np.int64)
+    row[N] = 65536
+    assert np.all(np.diff(row) >= 1) and row[2] == 2
+    rows = np.broadcast_to(row, (C, N + 1)).astype(np.uint32)
+    streams, lengths = [], []
+    syms = np.zeros((2, L, T, C), dtype=np.uint8)
+    for kv in range(2):
+        for t in range(T):
+            s = rng.integers(2, N - 1, C)              # common symbols 2..14
+            if t % 3 == 0:
+                s[: C // 2] = rng.integers(0, 2, C // 2)  # a run of the rare ones
+            elif t % 3 == 1:
+                s[5:9] = 0                              # one rare batch
+            syms[kv, 0, t] = s
+            b = orc.wnc_encode(s, rows)
+            streams.append(b)
+            lengths.append(len(b))
+    wire = np.tile(row.astype(np.uint32) & 0xFFFF, (2 * C, 1)).astype(np.uint16).ravel()
+    enc = {"amax": rng.uniform(0.5, 2.0, (2, L, T)).astype(np.float32),
+           "lengths": np.array(lengths, dtype=np.int32), "cdf": wire,
+           "bytes": np.frombuffer(b"".join(streams), dtype=np.uint8),
+           "stream_bytes": sum(lengths)}
+    k = v = [(0, L, N)]
+    want, sym = orc.decode(enc, L, T, C, 256, k, v, want_symbols=True)
+    assert np.array_equal(sym, syms)
+    blob = orc.serialize(enc, L, T, H, D, 256, k, v)
+    codec, e = cg.Codec.from_bytes(torch.from_numpy(np.frombuffer(blob, np.uint8).copy()))
+    out = codec.decode(e)
+    assert np.array_equal(_bits(out).reshape(L, 2, T, C), want)
