@@ -872,21 +872,25 @@ __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t
         for (int j = 0; j < 8; ++j) {
             // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's
             // own comparison, so the result is exact)
-            uint32_t s = 0;
+            // (sb = 2s, the position as a byte offset into the row: every
+            // probe is then base + offset + constant)
+            const char *rb = reinterpret_cast<const char *>(row);
+            uint32_t sb = 0;
             if (NB > 0 && (NB & (NB - 1)) == 0) {
 #pragma unroll
                 for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
-                    if (scale16(d, row[s + step]) <= v)
-                        s += step;
+                    if (scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step)) <= v)
+                        sb += 2 * step;
             } else {
                 for (uint32_t step = top_step; step != 0; step >>= 1) {
-                    const uint32_t t = s + step;
-                    if (t < (uint32_t)N && scale16(d, row[t]) <= v)
-                        s = t;
+                    const uint32_t t = sb + 2 * step;
+                    if (t < 2 * (uint32_t)N &&
+                        scale16(d, *reinterpret_cast<const uint16_t *>(rb + t)) <= v)
+                        sb = t;
                 }
             }
-            const uint32_t c0v = row[s];
-            const uint32_t c1r = row[s + 1];  // 0 stands for 65536
+            const uint32_t c0v = *reinterpret_cast<const uint16_t *>(rb + sb);
+            const uint32_t c1r = *reinterpret_cast<const uint16_t *>(rb + sb + 2);  // 0: 65536
             const uint32_t t0 = scale16(d, c0v);
             const uint32_t t1 = (c1r == 0) ? d + 1u : scale16(d, c1r);
             const uint32_t dn = t1 - t0 - 1u;
@@ -912,7 +916,8 @@ __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t
             }
             // dequantise: bf16(fp32((q - MAX) / MAX) * a), two values per
             // conversion (each rounded to nearest even on its own)
-            const float y = __fmul_rn(deq[s], a);
+            const float y =
+                __fmul_rn(*reinterpret_cast<const float *>(reinterpret_cast<const char *>(deq) + 2 * sb), a);
             if (j & 1) {
                 const __nv_bfloat162 pr = __floats2bfloat162_rn(y_even, y);
                 packed[j >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
