@@ -889,11 +889,14 @@ __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t
                         sb = t;
                 }
             }
+            // a valid stream never holds the top symbol N - 1 (never coded);
+            // clamping keeps a corrupt one below it, so cdf[s + 1] is an
+            // interior entry (1..65535) and the bounds stay well formed
+            sb = min(sb, 2u * (uint32_t)(N - 2));
             const uint32_t c0v = *reinterpret_cast<const uint16_t *>(rb + sb);
-            const uint32_t c1r = *reinterpret_cast<const uint16_t *>(rb + sb + 2);  // 0: 65536
+            const uint32_t c1v = *reinterpret_cast<const uint16_t *>(rb + sb + 2);
             const uint32_t t0 = scale16(d, c0v);
-            const uint32_t t1 = (c1r == 0) ? d + 1u : scale16(d, c1r);
-            const uint32_t dn = t1 - t0 - 1u;
+            const uint32_t dn = scale16(d, c1v) - t0 - 1u;
             // renormalise (see Enc); v takes S new bits
             const uint32_t xs = x + t0;
             const uint32_t hs = xs + dn;
