@@ -399,7 +399,8 @@ __device__ __noinline__ uint64_t code_stream_exact(const uint8_t *srow8, int32_t
 }
 
 // Phase A, counting one block of rows: each thread owns W consecutive
-// channels (W = 2: channel pairs with 4-byte loads; W = 1 for narrow rows).
+// channels (W = 4 with 8-byte loads and 4-byte symbol stores; W = 2 and 1
+// for narrower rows).
 template <int W>
 __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, int32_t C,
                                             int32_t r0, int32_t nr, const float *fac, float fmax,
@@ -410,7 +411,30 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
         uint16_t *h0 = table + (size_t)(W * p) * Lp;
         for (int32_t rb = r0; rb < r0 + nr; rb += kCountBatch) {
             const int32_t nb = min(kCountBatch, r0 + nr - rb);
-            if (W == 2) {
+            if (W == 4) {
+                const uint2 *src = reinterpret_cast<const uint2 *>(rows) + p;
+                uint32_t *dst = reinterpret_cast<uint32_t *>(sym_tile) + p;
+                uint2 w[kCountBatch];
+#pragma unroll
+                for (int u = 0; u < kCountBatch; ++u)
+                    w[u] = (u < nb) ? __ldg(src + (size_t)(rb + u) * (C / 4)) : make_uint2(0u, 0u);
+#pragma unroll
+                for (int u = 0; u < kCountBatch; ++u) {
+                    if (u < nb) {
+                        const float f = fac[rb + u];
+                        const uint32_t q0 = quantise(__uint_as_float(w[u].x << 16), f, fmax);
+                        const uint32_t q1 = quantise(__uint_as_float(w[u].x & 0xFFFF0000u), f, fmax);
+                        const uint32_t q2 = quantise(__uint_as_float(w[u].y << 16), f, fmax);
+                        const uint32_t q3 = quantise(__uint_as_float(w[u].y & 0xFFFF0000u), f, fmax);
+                        h0[q0] += 1;
+                        h0[Lp + q1] += 1;
+                        h0[2 * Lp + q2] += 1;
+                        h0[3 * Lp + q3] += 1;
+                        dst[(size_t)(rb + u) * (C / 4)] =
+                            __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
+                    }
+                }
+            } else if (W == 2) {
                 const uint32_t *src = reinterpret_cast<const uint32_t *>(rows) + p;
                 uint16_t *dst = reinterpret_cast<uint16_t *>(sym_tile) + p;
                 uint32_t w[kCountBatch];
@@ -574,7 +598,9 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
         uint4 xa[4];
         if (pipelined)
             amax_issue(rows + (size_t)ta * C, C, ta < tl.n, xa);
-        if (C / 2 >= NT)
+        if (C / 4 >= NT)
+            count_block<4>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
+        else if (C / 2 >= NT)
             count_block<2>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
         else
             count_block<1>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
