@@ -147,9 +147,9 @@ def kernel_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu capture, if it was taken
-    on the current kernel source; else None."""
+def recorded_counter(kernel: str, workload: str, key: str = "dram_bytes_per_launch"):
+    """A per-launch counter (DRAM bytes, warp instructions) from a committed
+    ncu capture, if it was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -159,20 +159,39 @@ def recorded_traffic(kernel: str, workload: str):
     e = d.get(kernel, {}).get(workload)
     if not e or e.get("source_sha") != kernel_source_hash():
         return None
-    return e.get("dram_bytes_per_launch")
+    return e.get(key)
+
+
+NOMINAL_SM_MHZ = 2070.0  # maximum SM clock of the part when nvidia-smi is unavailable
+
+
+def issue_ceiling(kernel: str, workload: str, ms_per_launch: float, sms: int, sm_mhz):
+    """The coders are bound by instruction issue, not HBM: warp instructions
+    per launch (ncu, current source) over the launch time, against one warp
+    instruction per scheduler per cycle (4 per SM) at the maximum SM clock."""
+    inst = recorded_counter(kernel, workload, "warp_instructions_per_launch")
+    mhz = float(sm_mhz) if sm_mhz else NOMINAL_SM_MHZ
+    peak = sms * 4 * mhz * 1e6
+    if inst is None:
+        return {"bound": "alu", "kernel": kernel, "achieved": None, "peak": peak,
+                "unit": "warp-instructions/s", "frac": None, "instructions_per_launch": None}
+    achieved = inst / (ms_per_launch * 1e-3)
+    return {"bound": "alu", "kernel": kernel, "achieved": round(achieved / 1e9, 2) * 1e9,
+            "peak": peak, "unit": "warp-instructions/s", "frac": round(achieved / peak, 4),
+            "instructions_per_launch": int(inst), "sm_mhz": mhz, "sms": sms}
 
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_sample(name: str, bits):
+def oracle_sample(name: str, bits, nthreads: int = 0):
     """Encode + decode a bounded sample (bits = the first tokens of the
-    workload) with the CPU oracle on all host cores. Returns (seconds, raw
-    bytes, threads, encoded)."""
+    workload) with the CPU oracle on nthreads host cores (0: all). Returns
+    (seconds, raw bytes, threads, encoded)."""
     from oracle import oracle
     p, k, v = workload_info(name)
     L, _, T, C = bits.shape
     ch = p["chunk_tokens"][0]
-    nth = oracle.max_threads()
+    nth = nthreads if nthreads > 0 else oracle.max_threads()
     t0 = time.perf_counter()
     enc = oracle.encode(bits, ch, k, v, nthreads=nth)
     oracle.decode(enc, L, T, C, ch, k, v, nthreads=nth)
@@ -181,13 +200,20 @@ def oracle_sample(name: str, bits):
 
 
 def cpu_baseline(name: str, tokens: int):
+    """The oracle on all host cores over the first `tokens` tokens, and on one
+    core over a sixteenth of them."""
     from kv_cache_compression_03_gb300 import synthetic
     bits = synthetic.generate(name, num_tokens=tokens)
     dt, raw, nth, _ = oracle_sample(name, bits)
+    t1 = max(1, tokens // 16)
+    dt1, raw1, _, _ = oracle_sample(name, bits[:, :, :t1].copy(), nthreads=1)
     p, _, _ = workload_info(name)
     return {"value": round(raw / dt / 1e9, 4), "unit": "GB/s", "cores": nth, "kind": "oracle",
             "sample": f"first {tokens} of {p['T']} tokens, all {p['L']} layers, K and V "
-                      f"({raw / 1e6:.1f} MB raw bf16), encode+decode, {dt:.2f} s wall"}
+                      f"({raw / 1e6:.1f} MB raw bf16), encode+decode, {dt:.2f} s wall",
+            "single_core": {"value": round(raw1 / dt1 / 1e9, 4), "unit": "GB/s",
+                            "sample": f"first {t1} tokens ({raw1 / 1e6:.1f} MB), "
+                                      f"{dt1:.2f} s wall"}}
 
 
 def run_reference(args):
@@ -474,7 +500,7 @@ def run_codec(args):
     per_launch_ms = kms / klaunch
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
-    traffic = recorded_traffic(kname, name)
+    traffic = recorded_counter(kname, name)
     roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -527,6 +553,8 @@ def run_codec(args):
     if rank != 0:
         return 0
     clocks = clk.summary()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    issue = issue_ceiling(kname, name, per_launch_ms, sms, (clocks or {}).get("sm_max_mhz"))
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -547,6 +575,7 @@ def run_codec(args):
         "kernels": {n: {"launches": c, "ms_per_launch": round(ms / c, 4)}
                     for n, (c, ms) in prof.items()},
         "roofline": roof,
+        "issue": issue,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "baselines": baselines,

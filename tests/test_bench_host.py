@@ -38,3 +38,17 @@ def test_sweep_settings_are_valid_spec_lists(orc):
             orc.layer_bins(L, k)   # raises on lists that do not tile [0, L)
             orc.layer_bins(L, v)
         assert "preset" in seen and "uniform16" in seen
+
+
+def test_issue_ceiling_arithmetic():
+    r = bench.issue_ceiling("no_such_kernel", "llama8b_t16k", 2.0, 152, 2070.0)
+    assert r["bound"] == "alu" and r["achieved"] is None and r["frac"] is None
+    assert r["peak"] == 152 * 4 * 2070e6
+    r = bench.issue_ceiling("no_such_kernel", "llama8b_t16k", 2.0, 100, None)
+    assert r["peak"] == 100 * 4 * bench.NOMINAL_SM_MHZ * 1e6
+
+
+def test_cpu_baseline_small_sample(orc):
+    c = bench.cpu_baseline("opt125m_t256", 32)
+    assert c["kind"] == "oracle" and c["value"] > 0 and c["cores"] >= 1
+    assert c["single_core"]["value"] > 0
