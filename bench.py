@@ -236,17 +236,18 @@ def run_reference(args):
     value = raw * len(times) / tot / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
-        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * tot / len(times), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "layers": p["L"], "tokens": p["T"],
                    "kv_heads": p["H"], "head_size": p["D"], "chunk_tokens": p["chunk_tokens"][0],
-                   "sample_tokens": tokens},
+                   "sample_tokens": tokens, "device": "host cores (CPU oracle)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nth,
                          "kind": "oracle",
                          "sample": f"first {tokens} of {p['T']} tokens per step, encode+decode"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "gpu_launches": 0, "clocks": None,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -500,7 +501,8 @@ def run_codec(args):
     per_launch_ms = kms / klaunch
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
-    traffic = recorded_counter(kname, name)
+    full_size = (T == p["T"])  # the recorded counters are per full-size launch
+    traffic = recorded_counter(kname, name) if full_size else None
     roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -554,7 +556,8 @@ def run_codec(args):
         return 0
     clocks = clk.summary()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    issue = issue_ceiling(kname, name, per_launch_ms, sms, (clocks or {}).get("sm_max_mhz"))
+    issue = issue_ceiling(kname, name if full_size else "", per_launch_ms, sms,
+                          (clocks or {}).get("sm_max_mhz"))
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),

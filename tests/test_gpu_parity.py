@@ -325,3 +325,36 @@ def test_decoder_batches_that_run_short(orc):
     codec, e = cg.Codec.from_bytes(torch.from_numpy(np.frombuffer(blob, np.uint8).copy()))
     out = codec.decode(e)
     assert np.array_equal(_bits(out).reshape(L, 2, T, C), want)
+
+
+def test_encode_decode_in_a_cuda_graph(orc):
+    """cg_encode and cg_decode (side-stream fork and join included) are
+    stream-ordered only, so they can be captured into a CUDA graph; replays
+    give the eager results."""
+    name = "mistral7b_t1k"
+    p = synthetic.WORKLOADS[name]
+    bits = synthetic.generate(name, num_tokens=300)
+    k, v = synthetic.workload_specs(name)
+    L, _, T, C = bits.shape
+    codec, kv, enc, out = _run(bits, p["H"], p["D"], 256, k, v)  # eager, and first-use setup
+    n = enc.stream_bytes
+    enc2 = codec.alloc_encoded()
+    out2 = torch.empty_like(out)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cg.cg_encode(codec.plan, kv, codec.workspace, enc2.bytestream, enc2.lengths, enc2.cdf,
+                     enc2.amax)
+        cg.cg_decode(codec.plan, enc2.bytestream, enc2.lengths, enc2.cdf, enc2.amax, n,
+                     codec.workspace, out2)
+    for _ in range(2):
+        out2.zero_()
+        enc2.bytestream.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        st, total = cg.cg_last_device_error(codec.plan, codec.workspace)
+        assert st == cg.CG_OK and total == n
+        assert torch.equal(enc2.bytestream[:n], enc.bytestream[:n])
+        assert torch.equal(enc2.lengths, enc.lengths) and torch.equal(enc2.cdf, enc.cdf)
+        assert torch.equal(out2, out)
+    ref = orc.encode(bits, 256, k, v)
+    assert np.array_equal(_bits(out2).reshape(L, 2, T, C), orc.decode(ref, L, T, C, 256, k, v))
