@@ -83,6 +83,11 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            # let sampling start before the timed region (a short region may
+            # otherwise end before nvidia-smi prints its first line)
+            t_end = time.perf_counter() + 3.0
+            while not self.lines and self.proc.poll() is None and time.perf_counter() < t_end:
+                time.sleep(0.005)
         except (OSError, ValueError):
             self.proc = None
         return self
