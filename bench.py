@@ -418,6 +418,66 @@ def run_bins_sweep(args):
     return 0
 
 
+def run_chunk_sweep(args):
+    """The chunk-size sweep workload: for each chunk_tokens, encode and decode
+    timed separately (device events), the ratio of the whole-blob container
+    and of the per-object containers, and the time to write all per-object
+    containers. One JSON line per chunk size."""
+    import numpy as np
+    import torch
+
+    from kv_cache_compression_03_gb300 import cachegen as cg
+    from kv_cache_compression_03_gb300 import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    name = "mistral7b_chunk_sweep"
+    p, k, v = workload_info(name)
+    L, T, H, D = p["L"], p["T"], p["H"], p["D"]
+    bits = synthetic.generate(name)
+    kv = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(L, 2, T, H, D).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    for ch in p["chunk_tokens"]:
+        codec = cg.Codec(L, T, H, D, ch, k, v, device=dev)
+        enc = codec.encode(kv)
+        out = codec.decode(enc)
+        raw = codec.sizes.raw_bytes
+        container = cg.cg_container_size(codec.plan, enc.stream_bytes)
+        for _ in range(args.warmup):
+            codec.encode(kv, enc, sync=False, stream=stream)
+            codec.decode(enc, out, sync=False, stream=stream)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for _ in range(args.steps):
+            codec.encode(kv, enc, sync=False, stream=stream)
+        ev[1].record(stream)
+        for _ in range(args.steps):
+            codec.decode(enc, out, sync=False, stream=stream)
+        ev[2].record(stream)
+        torch.cuda.synchronize(dev)
+        st, _ = cg.cg_last_device_error(codec.plan, codec.workspace)
+        assert st == cg.CG_OK, st
+        t_e = ev[0].elapsed_time(ev[1]) / args.steps
+        t_d = ev[1].elapsed_time(ev[2]) / args.steps
+        t0 = time.perf_counter()
+        objs = codec.object_bytes(enc)
+        t_obj = time.perf_counter() - t0
+        obj_bytes = sum(int(o.numel()) for o in objs)
+        line = {"sweep": "chunk_tokens", "workload": name, "tokens": T, "chunk_tokens": ch,
+                "groups": codec.sizes.num_groups, "objects": len(objs),
+                "encode_gbs": round(raw / (t_e * 1e-3) / 1e9, 2),
+                "decode_gbs": round(raw / (t_d * 1e-3) / 1e9, 2),
+                "encode_ms": round(t_e, 4), "decode_ms": round(t_d, 4),
+                "compression_ratio": round(raw / container, 4),
+                "per_object_ratio": round(raw / obj_bytes, 4),
+                "per_object_serialize_ms": round(1e3 * t_obj, 3),
+                "l2": "the whole blob (%.1f MB) fits in L2" % (raw / 1e6)}
+        print(json.dumps(line), flush=True)
+        del codec, enc, out
+    return 0
+
+
 def run_codec(args):
     import numpy as np
     import torch
@@ -615,11 +675,16 @@ def main():
     ap.add_argument("--sweep-bins", action="store_true",
                     help="instead of the benchmark line: ratio vs reconstruction error for "
                          "several bin settings, one JSON line each")
+    ap.add_argument("--sweep-chunks", action="store_true",
+                    help="instead of the benchmark line: the chunk-size sweep workload, "
+                         "one JSON line per chunk_tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.sweep_bins:
         return run_bins_sweep(args)
+    if args.sweep_chunks:
+        return run_chunk_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_codec(args)
