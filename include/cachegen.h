@@ -54,6 +54,12 @@
  *                16-byte aligned
  *     bytestream uint8, the concatenated streams, 16-byte aligned
  *
+ * Threads: a plan holds a side stream and two events with which cg_encode
+ * and cg_decode fork work onto a second stream and join it back. Calls that
+ * use the same plan must therefore come from one host thread at a time (use
+ * one plan per thread); calls on different plans are independent. Device
+ * work of two calls may overlap only if they use different workspaces.
+ *
  * Errors: argument and configuration errors are returned synchronously.
  * Errors found on the device (capacity exceeded, non-finite input, a
  * corrupt container) set a status word in the workspace; read it with
