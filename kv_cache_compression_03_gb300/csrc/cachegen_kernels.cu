@@ -7,24 +7,31 @@
 // of Witten, Neal & Cleary, CACM 30(6), 1987.
 //
 // Work decomposition: one CTA of 256 threads per tile = (token group,
-// K/V, layer), all tiles in one launch ordered by bin count, largest
-// first; each CTA branches (uniformly) into a body specialised for 16 or
-// 32 bins, or a generic one. Encode (then a tile scan and a pack):
+// K/V, layer). Tiles are grouped by bin count; each group is one launch of
+// a kernel specialised for 16 or 32 bins (or a generic one) with its own
+// shared-memory size and CTAs per SM, and the launches of one call run
+// concurrently on the caller's stream and a forked side stream. Encode
+// (then a tile scan and a pack):
 //   A  blocks of 8 token rows: warp per row computes amax over the C
 //      channels (16-byte loads; |x| maximum on bf16 bit patterns) and the
-//      row's scale factor; then thread per channel (pair) re-reads the
+//      row's scale factor; then a thread per four channels re-reads the
 //      block (L1/L2-resident), quantises, counts into its own shared-memory
 //      histogram rows (no atomics) and writes the symbols to a scratch row
 //      per stream. The next block's amax overlaps this block's counting.
 //   B  thread per channel: integer CDF in place of the histogram, copied
 //      out as the tile's CDF block.
 //   C  thread per token: arithmetic-code the token's stream over the C
-//      channels with the shared-memory CDF rows (see Enc).
+//      channels with the shared-memory CDF rows (see Enc); completed words
+//      are taken out of the bit buffer once per kStoreEvery symbols.
 // Pack: block scan of the tile's lengths + the tile's base, then the
 // slots are copied to their packed position. Decode: per tile, the CDF
 // block is staged in shared memory, the lengths are scanned, and each
 // thread decodes one stream (binary search with the coder's exact
-// comparison) and writes the dequantised bf16 row.
+// comparison; the bit buffer refilled once per kRefillEvery symbols) and
+// writes the dequantised bf16 row. A stream whose batch of symbols over- or
+// under-runs the 64-bit bit buffer (possible only for runs of a group's
+// rarest symbols) is redone on an exact path that checks after every
+// symbol.
 //
 // No kernel waits on another block, and every loop is bounded by the
 // tile's token and channel counts or the alphabet size.
