@@ -147,9 +147,20 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def code_hash(text: str) -> str:
+    """sha256 of C/CUDA source with comments and whitespace removed, so that
+    an edit of comments alone keeps the hash (string literals in the kernel
+    source hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"\s+", "", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def kernel_source_hash() -> str:
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(KERNEL_SOURCE, encoding="utf-8") as f:
+        return code_hash(f.read())
 
 
 def recorded_counter(kernel: str, workload: str, key: str = "dram_bytes_per_launch"):

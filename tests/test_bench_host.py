@@ -52,3 +52,18 @@ def test_cpu_baseline_small_sample(orc):
     c = bench.cpu_baseline("opt125m_t256", 32)
     assert c["kind"] == "oracle" and c["value"] > 0 and c["cores"] >= 1
     assert c["single_core"]["value"] > 0
+
+
+def test_code_hash_ignores_comments_only():
+    a = "int f(int x) { return x + 1; } // one\n/* two */\n"
+    b = "int f(int x)\n{\n    return x + 1;  /* changed */\n}\n"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.code_hash(a) == bench.code_hash(b)
+    assert bench.code_hash(a) != bench.code_hash(c)
+
+
+def test_recorded_counters_match_the_kernel_source():
+    # the committed ncu counters were taken on the current kernel code
+    assert bench.recorded_counter("k_decode_tiles", "llama8b_t16k") is not None
+    assert bench.recorded_counter("k_encode_tiles", "llama8b_t16k",
+                                  "warp_instructions_per_launch") is not None
