@@ -767,8 +767,37 @@ __global__ void __launch_bounds__(NT)
             continue;
         }
         const uint8_t *src = slots + (tl.first_stream + i) * (uint64_t)P.slot_stride + 16;
-        for (uint32_t b = lane; b < li; b += 32)
-            bytestream[dst + b] = src[b];
+        // bytes up to the first 4-byte boundary of the destination and after
+        // its last one go byte by byte (those words may hold a neighbouring
+        // stream's bytes); the body goes as whole words, each taken from two
+        // aligned source words by a funnel shift (the slot is 16-byte aligned
+        // and holds a multiple of 4 bytes, so no read leaves it)
+        const uint32_t h = min((4u - (uint32_t)(dst & 3u)) & 3u, li);
+        const uint32_t nw = (li - h) >> 2;
+        const uint32_t t0 = h + 4u * nw;
+        if (lane < h)
+            bytestream[dst + lane] = src[lane];
+        if (lane < li - t0)
+            bytestream[dst + t0 + lane] = src[t0 + lane];
+        uint32_t *d32 = reinterpret_cast<uint32_t *>(bytestream + dst + h);
+        const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);
+        // up to four words per lane loaded before any is stored: one load
+        // latency per 512 bytes of stream
+        for (uint32_t j0 = 0; j0 < nw; j0 += 128) {
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t j = j0 + lane + 32u * k;
+                lo[k] = (j < nw) ? s32[j] : 0u;
+                hi[k] = (j < nw && h) ? s32[j + 1] : 0u;  // bytes h + 4j .. h + 4j + 3
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t j = j0 + lane + 32u * k;
+                if (j < nw)
+                    d32[j] = __funnelshift_r(lo[k], hi[k], 8u * h);
+            }
+        }
     }
 }
 
