@@ -63,3 +63,30 @@ def test_codec_arm_line():
     assert b["int8"]["compression_ratio"] == pytest.approx(2 * 1024 / 1028, rel=1e-3)
     assert b["naive"]["compression_ratio"] == 1.0
     assert set(b["transfer_model"]) >= {"bandwidth_mbps", "raw_s", "cachegen_s", "int8_s"}
+
+
+def _lines(args, timeout=900):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+
+
+@pytest.mark.gpu
+def test_bins_sweep_lines():
+    rows = _lines(["--sweep-bins", "--tokens", "256", "--steps", "2", "--warmup", "3"])
+    by = {r["setting"]: r for r in rows}
+    assert {"preset", "uniform8", "uniform16", "uniform32", "uniform64"} <= set(by)
+    # more bins: lower error, lower ratio
+    assert by["uniform8"]["rel_rmse"] > by["uniform16"]["rel_rmse"] > by["uniform32"]["rel_rmse"]
+    assert by["uniform8"]["compression_ratio"] > by["uniform16"]["compression_ratio"] \
+        > by["uniform32"]["compression_ratio"]
+
+
+@pytest.mark.gpu
+def test_chunk_sweep_lines():
+    rows = _lines(["--sweep-chunks", "--steps", "2", "--warmup", "3"])
+    assert [r["chunk_tokens"] for r in rows] == [64, 128, 256, 768]
+    for r in rows:
+        assert abs(r["per_object_ratio"] - r["compression_ratio"]) < 1e-3 * r["compression_ratio"]
+        assert r["objects"] == -(-768 // r["chunk_tokens"])
