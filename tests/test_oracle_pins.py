@@ -2,7 +2,6 @@
 hand-derived fixtures (tests/golden), closed forms, invariants, an
 exact-rational model of the coder, and brute force on tiny inputs."""
 import itertools
-import math
 import os
 
 import numpy as np
