@@ -12,7 +12,7 @@
 // shared-memory size and CTAs per SM, and the launches of one call run
 // concurrently on the caller's stream and a forked side stream. Encode
 // (then a tile scan and a pack):
-//   A  blocks of 8 token rows: warp per row computes amax over the C
+//   A  blocks of 16 token rows: warp per row computes amax over the C
 //      channels (16-byte loads; |x| maximum on bf16 bit patterns) and the
 //      row's scale factor; then a thread per four channels re-reads the
 //      block (L1/L2-resident), quantises, counts into its own shared-memory
@@ -46,7 +46,7 @@
 namespace {
 
 constexpr int NT = CG_TILE_THREADS;
-constexpr int kRowsPerBlock = 8;   // encoder phase A block (one row per warp)
+constexpr int kRowsPerBlock = 16;  // encoder phase A block (two rows per warp)
 constexpr int kCountBatch = 8;     // rows whose loads a counting thread keeps in flight
 
 __device__ __forceinline__ void set_status(uint32_t *st, uint32_t code)
@@ -592,8 +592,9 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     // A: amax of block 0; then per step, count block b while the loads for
     // block b + 1's amax are in flight (one row per warp), and ask L2 for
     // block b + 2
-    if (warp < tl.n)
-        row_amax(rows + (size_t)warp * C, C, fmax, &fac[warp], &amax_row[warp], nonfinite);
+    for (int32_t rr = warp; rr < kRowsPerBlock; rr += NT / 32)
+        if (rr < tl.n)
+            row_amax(rows + (size_t)rr * C, C, fmax, &fac[rr], &amax_row[rr], nonfinite);
     __syncthreads();
     const bool pipelined = (C <= 1024);
     for (int32_t b = 0; b < nblocks; ++b) {
@@ -615,6 +616,9 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
             amax_finish(xa, ta < tl.n, fmax, &fac[ta], &amax_row[ta], nonfinite);
         else if (ta < tl.n)
             row_amax(rows + (size_t)ta * C, C, fmax, &fac[ta], &amax_row[ta], nonfinite);
+        const int32_t tb = ta + NT / 32;
+        if (tb < tl.n)
+            row_amax(rows + (size_t)tb * C, C, fmax, &fac[tb], &amax_row[tb], nonfinite);
         __syncthreads();
     }
     if (tid == 0 && *nonfinite)
