@@ -155,6 +155,18 @@ void cg_plan_destroy(cg_plan *plan);
 /* Fill *out with the buffer sizes of a plan. Host only. */
 cg_status cg_plan_sizes(const cg_plan *plan, cg_sizes *out);
 
+/* The configuration a plan was built from (for a plan from
+ * cg_container_open: the shape, chunk_tokens and spec lists recorded in the
+ * container, which from_bytes of [CG-LMCache §5] must recover). Host only.
+ * out gets the five sizes and n_kspecs / n_vspecs; its kspecs / vspecs
+ * point at the caller's arrays kspecs[kcap] and vspecs[vcap], which receive
+ * the spec triples in the order they were given. If kcap < n_kspecs or
+ * vcap < n_vspecs nothing is copied and CG_ERR_CAPACITY is returned (the
+ * counts are still set, so a caller can size its arrays and call again);
+ * a NULL array is allowed with a capacity of 0. */
+cg_status cg_plan_config(const cg_plan *plan, cg_config *out, cg_quant_spec *kspecs,
+                         int32_t kcap, cg_quant_spec *vspecs, int32_t vcap);
+
 /* Encode kv (device, bf16 [L][2][T][H*D]) into out's device buffers
  * [CG-LMCache §2-§4]. workspace (device, >= workspace_bytes, 256-byte
  * aligned) is scratch; its first 256 bytes receive the device status and
@@ -274,12 +286,18 @@ cg_status cg_deserialize_objects(const cg_plan *plan, int32_t num_objects,
  * kv and the output buffers (same rules as cg_encode) and status_out, a
  * device buffer of at least 16 bytes that receives the device status word
  * and the total stream bytes (read it with cg_last_device_error, passing
- * status_out as the workspace). The first call on each device looks up the
- * array's device address (with that device current); make that first call
- * before any stream capture. All calls share the one array and it keeps the
- * last call's contents (each call clears what must start at zero): calls
- * that can overlap on the GPU, from any stream or thread, race on it, so
- * serialise them. Asynchronous on stream. */
+ * status_out as the workspace). Every call looks up the array's device
+ * address in the current device's context (nothing is cached, so a device
+ * reset leaves no stale address); the first call on each device also loads
+ * the library's device code there, so make that first call before any
+ * stream capture. All calls share the one array and it keeps the last
+ * call's contents (each call clears what must start at zero): calls that
+ * can overlap on the GPU, from any stream or thread, race on it, so
+ * serialise them. status_out is not a workspace: the object calls
+ * (cg_object_streams, cg_serialize_object) read tile offsets that only a
+ * cg_encode workspace holds, so they must not be given status_out; encode
+ * with cg_encode when per-object containers are needed. Asynchronous on
+ * stream. */
 cg_status cg_encode_noalloc(const cg_plan *plan, const void *kv, const cg_encoded *out,
                             void *status_out, cg_stream_t stream);
 

@@ -85,6 +85,8 @@ def load(build_if_missing: bool = True) -> ct.CDLL:
             "cg_plan_create": (st, [ct.POINTER(cg_config), ct.POINTER(ct.c_void_p)]),
             "cg_plan_destroy": (None, [P]),
             "cg_plan_sizes": (st, [P, ct.POINTER(cg_sizes)]),
+            "cg_plan_config": (st, [P, ct.POINTER(cg_config), ct.POINTER(cg_quant_spec),
+                                    ct.c_int32, ct.POINTER(cg_quant_spec), ct.c_int32]),
             "cg_encode": (st, [P, P, P, sz, ct.POINTER(cg_encoded), P]),
             "cg_decode": (st, [P, ct.POINTER(cg_encoded), u64, P, sz, P, P]),
             "cg_last_device_error": (st, [P, P, ct.POINTER(ct.c_int), ct.POINTER(u64), P]),
@@ -132,6 +134,15 @@ def _ptr(t) -> int:
     return t.data_ptr() if t is not None else 0
 
 
+def _check_status_buffer(status_out, what: str) -> None:
+    """The C side copies a 16-byte status block into status_out: it must be
+    a CUDA tensor of at least 16 bytes (a smaller one would be overrun)."""
+    if status_out is None or not getattr(status_out, "is_cuda", False):
+        raise ValueError(f"{what}: status_out must be a CUDA tensor")
+    if status_out.numel() * status_out.element_size() < 16:
+        raise ValueError(f"{what}: status_out must hold at least 16 bytes")
+
+
 # ------------------------------------------------------------ C ABI mirror
 
 def cg_status_string(status: int) -> str:
@@ -169,6 +180,25 @@ def cg_plan_sizes(plan) -> cg_sizes:
     return s
 
 
+def cg_plan_config(plan):
+    """The configuration of a plan: (num_layers, num_tokens, num_heads,
+    head_size, chunk_tokens, kspecs, vspecs) with the specs as
+    (start_layer, end_layer, bins) triples."""
+    lib = load()
+    cfg = cg_config()
+    st = lib.cg_plan_config(ct.c_void_p(plan), ct.byref(cfg), None, 0, None, 0)
+    if st not in (CG_OK, CG_ERR_CAPACITY):
+        _check(st, "cg_plan_config")
+    ka = (cg_quant_spec * max(cfg.n_kspecs, 1))()
+    va = (cg_quant_spec * max(cfg.n_vspecs, 1))()
+    _check(lib.cg_plan_config(ct.c_void_p(plan), ct.byref(cfg), ka, cfg.n_kspecs, va,
+                              cfg.n_vspecs), "cg_plan_config")
+    ks = [(ka[i].start_layer, ka[i].end_layer, ka[i].bins) for i in range(cfg.n_kspecs)]
+    vs = [(va[i].start_layer, va[i].end_layer, va[i].bins) for i in range(cfg.n_vspecs)]
+    return (cfg.num_layers, cfg.num_tokens, cfg.num_heads, cfg.head_size, cfg.chunk_tokens,
+            ks, vs)
+
+
 def _encoded_struct(bytestream, lengths, cdf, amax) -> cg_encoded:
     return cg_encoded(_ptr(bytestream), bytestream.numel() * bytestream.element_size(),
                       _ptr(lengths), _ptr(cdf), _ptr(amax))
@@ -186,6 +216,7 @@ def cg_encode_noalloc(plan, kv, bytestream, lengths, cdf, amax, status_out, stre
     (see include/cachegen.h). status_out: a device tensor of >= 16 bytes that
     receives the status word and total stream bytes; read it with
     cg_last_device_error(plan, status_out)."""
+    _check_status_buffer(status_out, "cg_encode_noalloc")
     enc = _encoded_struct(bytestream, lengths, cdf, amax)
     _check(load().cg_encode_noalloc(ct.c_void_p(plan), ct.c_void_p(_ptr(kv)), ct.byref(enc),
                                     ct.c_void_p(_ptr(status_out)), _stream_handle(stream)),
@@ -205,6 +236,7 @@ def cg_int8_encode(kv, rows, channels, q_out, scales_out, status_out, stream=Non
     into q_out int8 [rows][channels] and scales_out fp32 [rows]; status_out
     (>= 16 bytes) gets the device status, read with
     cg_last_device_error(None, status_out)."""
+    _check_status_buffer(status_out, "cg_int8_encode")
     _check(load().cg_int8_encode(ct.c_void_p(_ptr(kv)), int(rows), int(channels),
                                  ct.c_void_p(_ptr(q_out)), ct.c_void_p(_ptr(scales_out)),
                                  ct.c_void_p(_ptr(status_out)), _stream_handle(stream)),
@@ -482,14 +514,10 @@ class Codec:
         """Open a container (uint8 CPU tensor); return (codec, encoded)."""
         plan, sb = cg_container_open(host_in)
         try:
-            import struct
-            hdr = bytes(host_in[:48].numpy())
-            L, T, H, D, ch, nk, nv = struct.unpack_from("<7i", hdr, 8)
-            raw = bytes(host_in[48:48 + 12 * (nk + nv)].numpy())
-            specs = [struct.unpack_from("<3i", raw, 12 * i) for i in range(nk + nv)]
+            L, T, H, D, ch, kspecs, vspecs = cg_plan_config(plan)
         finally:
             cg_plan_destroy(plan)
-        codec = Codec(L, T, H, D, ch, specs[:nk], specs[nk:], device=device)
+        codec = Codec(L, T, H, D, ch, kspecs, vspecs, device=device)
         enc = codec.alloc_encoded(capacity=max(16, sb))
         enc.stream_bytes = sb
         cg_deserialize(codec.plan, host_in, enc.bytestream, enc.lengths, enc.cdf, enc.amax,

@@ -352,6 +352,29 @@ cg_status cg_plan_sizes(const cg_plan *p, cg_sizes *out)
     return CG_OK;
 }
 
+cg_status cg_plan_config(const cg_plan *p, cg_config *out, cg_quant_spec *kspecs, int32_t kcap,
+                         cg_quant_spec *vspecs, int32_t vcap)
+{
+    if (p == nullptr || out == nullptr || kcap < 0 || vcap < 0)
+        return CG_ERR_INVALID_ARG;
+    if ((kcap > 0 && kspecs == nullptr) || (vcap > 0 && vspecs == nullptr))
+        return CG_ERR_INVALID_ARG;
+    out->num_layers = p->L;
+    out->num_tokens = p->T;
+    out->num_heads = p->H;
+    out->head_size = p->D;
+    out->chunk_tokens = p->chunk_tokens;
+    out->n_kspecs = (int32_t)p->kspecs.size();
+    out->n_vspecs = (int32_t)p->vspecs.size();
+    out->kspecs = kspecs;
+    out->vspecs = vspecs;
+    if (kcap < out->n_kspecs || vcap < out->n_vspecs)
+        return CG_ERR_CAPACITY;
+    std::copy(p->kspecs.begin(), p->kspecs.end(), kspecs);
+    std::copy(p->vspecs.begin(), p->vspecs.end(), vspecs);
+    return CG_OK;
+}
+
 cg_status cg_encode(const cg_plan *p, const void *kv, void *workspace, size_t workspace_bytes,
                     const cg_encoded *out, cg_stream_t stream)
 {

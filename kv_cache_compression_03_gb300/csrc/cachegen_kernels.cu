@@ -139,13 +139,29 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
 
 // ------------------------------------------------------------ quantiser
 
-// q = round_half_even(fp32(fp32(x * f) + MAX)). For finite rows q lies in
-// [0, 2*MAX]; rows without a usable factor get f = 0 (row_factor), and the
-// conversion of NaN gives 0, so q stays in range for them too (they are
-// reported separately).
-__device__ __forceinline__ uint32_t quantise(float x, float f, float fmax)
+// q = round_half_even(fp32(fp32(x * f) + MAX)), for finite rows in
+// [0, 2*MAX]. The rounding to an integer is one more fp32 addition: y + 1.5 *
+// 2^23 lies in [2^23, 2^24), where the spacing of fp32 values is 1, so the
+// sum rounds y to the nearest integer with ties to even (1.5 * 2^23 is even)
+// and its low mantissa bits hold q (the constant's low 22 bits are zero).
+// This keeps the conversion on the FMA pipes instead of the slow
+// conversion unit. Returns the sum's bits; the caller masks out q.
+__device__ __forceinline__ uint32_t quantise_bits(float x, float f, float fmax)
 {
-    return (uint32_t)__float2int_rn(__fadd_rn(__fmul_rn(x, f), fmax));
+    return __float_as_uint(__fadd_rn(__fadd_rn(__fmul_rn(x, f), fmax), 12582912.0f));
+}
+
+// q from quantise_bits. Rows without a usable factor get f = 0 (row_factor)
+// and are reported separately; their inf/NaN values give NaN (0 * inf),
+// whose bits are not of the form above: the mask keeps q inside the
+// alphabet [0, N) for them too (N a power of two: the low log2 N bits;
+// otherwise at most N - 1).
+template <int NB>
+__device__ __forceinline__ uint32_t symbol_of(uint32_t bits, int32_t N)
+{
+    if (NB > 0 && (NB & (NB - 1)) == 0)
+        return bits & (uint32_t)(NB - 1);
+    return min(bits & 63u, (uint32_t)(N - 1));
 }
 
 // Scale factor MAX / a of a row whose largest |x| has bf16 bits m. A row
@@ -167,6 +183,41 @@ __device__ __forceinline__ float row_factor(uint32_t m, float fmax, uint32_t *no
 __device__ __forceinline__ uint32_t scale16(uint32_t d, uint32_t c)
 {
     return (uint32_t)(((uint64_t)d * c + c) >> 16);
+}
+
+// Shifts whose amount may reach 32 (a corrupt stream in the decoder): the
+// PTX shifts clamp the amount, so the result is defined (0).
+__device__ __forceinline__ uint32_t shl_clamped(uint32_t x, uint32_t s)
+{
+    uint32_t r;
+    asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(s));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t shr_clamped(uint32_t x, uint32_t s)
+{
+    uint32_t r;
+    asm("shr.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(s));
+    return r;
+}
+
+// Renormalisation shift of an interval whose low end (window) is xs and
+// whose width - 1 is dn: the number of times the textbook coder doubles the
+// interval after this symbol. Renormalisation stops once the width exceeds
+// a quarter of the window (2^30) while the interval straddles the middle
+// but not the middle half; the width after S doublings is (dn + 1) * 2^S,
+// and doubling stops within the first two octaves above 2^30, so S is
+// 30 - m or 31 - m with m = msb(dn). After 30 - m doublings the width lies
+// in (2^30, 2^31]: the ends xs, hs = xs + dn then sit in quarters whose
+// indices differ by 1 or 2, and one more doubling is due exactly when they
+// differ by 1 (both ends in one half, or in the middle half), i.e. when bit
+// m of xs ^ hs is set. One FLO instead of the two leading-zero counts of
+// the textbook bit-by-bit form.
+__device__ __forceinline__ uint32_t renorm_shift(uint32_t xs, uint32_t dn)
+{
+    uint32_t m;
+    asm("bfind.u32 %0, %1;" : "=r"(m) : "r"(dn));
+    return 30u - m + (shr_clamped(xs ^ (xs + dn), m) & 1u);
 }
 
 // ------------------------------------------------------------ encoder
@@ -280,13 +331,10 @@ __device__ __forceinline__ void enc_symbol(Enc &e, uint32_t c0, uint32_t c1)
     const uint32_t t1 = scale16(e.d, c1);
     const uint32_t xs = add_with_carry(e.x, t0, e.a0, e.a1);
     const uint32_t dn = t1 - t0 - 1u;  // new range - 1
-    const uint32_t hs = xs + dn;       // window of the high end
-    const uint32_t n = __clz(xs ^ hs);
-    const uint32_t k = __clz((~xs | hs) << (n + 1u));
-    const uint32_t S = n + k;
+    const uint32_t S = renorm_shift(xs, dn);
     e.a1 = __funnelshift_l(e.a0, e.a1, S);
     e.a0 = __funnelshift_l(xs, e.a0, S);
-    e.x = xs << S;
+    e.x = shl_clamped(xs, S);
     e.d = __funnelshift_l(0xFFFFFFFFu, dn, S);
     e.nb += S;
     if (STORE) {
@@ -408,11 +456,12 @@ __device__ __noinline__ uint64_t code_stream_exact(const uint8_t *srow8, int32_t
 // Phase A, counting one block of rows: each thread owns W consecutive
 // channels (W = 4 with 8-byte loads and 4-byte symbol stores; W = 2 and 1
 // for narrower rows).
-template <int W>
+template <int NB, int W>
 __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, int32_t C,
                                             int32_t r0, int32_t nr, const float *fac, float fmax,
-                                            uint16_t *table, int32_t Lp, uint8_t *sym_tile)
+                                            uint16_t *table, int32_t N, uint8_t *sym_tile)
 {
+    const int32_t Lp = N + 1;
     const int32_t units = C / W;
     for (int32_t p = threadIdx.x; p < units; p += NT) {
         uint16_t *h0 = table + (size_t)(W * p) * Lp;
@@ -429,10 +478,10 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
                 for (int u = 0; u < kCountBatch; ++u) {
                     if (u < nb) {
                         const float f = fac[rb + u];
-                        const uint32_t q0 = quantise(__uint_as_float(w[u].x << 16), f, fmax);
-                        const uint32_t q1 = quantise(__uint_as_float(w[u].x & 0xFFFF0000u), f, fmax);
-                        const uint32_t q2 = quantise(__uint_as_float(w[u].y << 16), f, fmax);
-                        const uint32_t q3 = quantise(__uint_as_float(w[u].y & 0xFFFF0000u), f, fmax);
+                        const uint32_t q0 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x << 16), f, fmax), N);
+                        const uint32_t q1 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x & 0xFFFF0000u), f, fmax), N);
+                        const uint32_t q2 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y << 16), f, fmax), N);
+                        const uint32_t q3 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y & 0xFFFF0000u), f, fmax), N);
                         h0[q0] += 1;
                         h0[Lp + q1] += 1;
                         h0[2 * Lp + q2] += 1;
@@ -452,8 +501,8 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
                 for (int u = 0; u < kCountBatch; ++u) {
                     if (u < nb) {
                         const float f = fac[rb + u];
-                        const uint32_t q0 = quantise(__uint_as_float(w[u] << 16), f, fmax);
-                        const uint32_t q1 = quantise(__uint_as_float(w[u] & 0xFFFF0000u), f, fmax);
+                        const uint32_t q0 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u] << 16), f, fmax), N);
+                        const uint32_t q1 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u] & 0xFFFF0000u), f, fmax), N);
                         h0[q0] += 1;
                         h0[Lp + q1] += 1;
                         dst[(size_t)(rb + u) * (C / 2)] = (uint16_t)(q0 | (q1 << 8));
@@ -469,7 +518,7 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
 #pragma unroll
                 for (int u = 0; u < kCountBatch; ++u) {
                     if (u < nb) {
-                        const uint32_t q = quantise(__uint_as_float(w[u] << 16), fac[rb + u], fmax);
+                        const uint32_t q = symbol_of<NB>(quantise_bits(__uint_as_float(w[u] << 16), fac[rb + u], fmax), N);
                         h0[q] += 1;
                         dst[(size_t)(rb + u) * C] = (uint8_t)q;
                     }
@@ -607,11 +656,11 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
         if (pipelined)
             amax_issue(rows + (size_t)ta * C, C, ta < tl.n, xa);
         if (C / 4 >= NT)
-            count_block<4>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
+            count_block<NB, 4>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
         else if (C / 2 >= NT)
-            count_block<2>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
+            count_block<NB, 2>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
         else
-            count_block<1>(rows, C, r0, nr, fac, fmax, table, Lp, sym_tile);
+            count_block<NB, 1>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
         if (pipelined)
             amax_finish(xa, ta < tl.n, fmax, &fac[ta], &amax_row[ta], nonfinite);
         else if (ta < tl.n)
@@ -878,11 +927,11 @@ __device__ __forceinline__ void bits_init(Bits &r, const uint8_t *bytestream, ui
     bits_refill(r);
 }
 
-// Drop S <= 18 bits.
+// Drop S bits (S <= 18 for a valid stream, <= 32 for a corrupt one).
 __device__ __forceinline__ void bits_skip(Bits &r, uint32_t S)
 {
     r.b1 = __funnelshift_l(r.b0, r.b1, S);
-    r.b0 <<= S;
+    r.b0 = shl_clamped(r.b0, S);
     r.avail -= (int32_t)S;
     bits_refill(r);
 }
@@ -937,46 +986,53 @@ __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's
-            // own comparison, so the result is exact)
+            // own comparison, so the result is exact), with r = d + 1 =
+            // 2^32 - e: r * c <= v * 2^16 + 0xFFFF  <=>  e * c + V >= c * 2^32
+            // for V = v * 2^16 + 0xFFFF, i.e. the high word of the 64-bit
+            // e * c + V is >= c (one wide multiply-add and one compare per
+            // probe; e fits 32 bits also when r = 2^32)
             // (sb = 2s, the position as a byte offset into the row: every
             // probe is then base + offset + constant)
             const char *rb = reinterpret_cast<const char *>(row);
+            const uint32_t e = ~d;
+            const uint64_t V = ((uint64_t)(v >> 16) << 32) | ((v << 16) | 0xFFFFu);
             uint32_t sb = 0;
             if (NB > 0 && (NB & (NB - 1)) == 0) {
 #pragma unroll
-                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
-                    if (scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step)) <= v)
+                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1) {
+                    const uint32_t c = *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step);
+                    if ((uint32_t)(((uint64_t)e * c + V) >> 32) >= c)
                         sb += 2 * step;
+                }
             } else {
                 for (uint32_t step = top_step; step != 0; step >>= 1) {
                     const uint32_t t = sb + 2 * step;
-                    if (t < 2 * (uint32_t)N &&
-                        scale16(d, *reinterpret_cast<const uint16_t *>(rb + t)) <= v)
-                        sb = t;
+                    if (t < 2 * (uint32_t)N) {
+                        const uint32_t c = *reinterpret_cast<const uint16_t *>(rb + t);
+                        if ((uint32_t)(((uint64_t)e * c + V) >> 32) >= c)
+                            sb = t;
+                    }
                 }
             }
-            // a valid stream never holds the top symbol N - 1 (never coded);
-            // clamping keeps a corrupt one below it, so cdf[s + 1] is an
-            // interior entry (1..65535) and the bounds stay well formed
-            sb = min(sb, 2u * (uint32_t)(N - 2));
+            // sb <= 2(N - 1), so both bounds lie in the row. A valid stream
+            // never holds the top symbol N - 1 (never coded); a corrupt one
+            // that reaches it gets cdf[N] (stored as 0) as its upper bound
+            // and decodes to garbage, still inside the buffers.
             const uint32_t c0v = *reinterpret_cast<const uint16_t *>(rb + sb);
             const uint32_t c1v = *reinterpret_cast<const uint16_t *>(rb + sb + 2);
             const uint32_t t0 = scale16(d, c0v);
             const uint32_t dn = scale16(d, c1v) - t0 - 1u;
             // renormalise (see Enc); v takes S new bits
             const uint32_t xs = x + t0;
-            const uint32_t hs = xs + dn;
-            const uint32_t n = __clz(xs ^ hs);
-            const uint32_t k = __clz((~xs | hs) << (n + 1u));
-            const uint32_t S = n + k;
-            x = xs << S;
+            const uint32_t S = renorm_shift(xs, dn);
+            x = shl_clamped(xs, S);
             d = __funnelshift_l(0xFFFFFFFFu, dn, S);
             v = __funnelshift_l(br.b1, v - t0, S);
             if (R == 1) {
                 bits_skip(br, S);
             } else {
                 br.b1 = __funnelshift_l(br.b0, br.b1, S);
-                br.b0 <<= S;
+                br.b0 = shl_clamped(br.b0, S);
                 br.avail -= (int32_t)S;
                 if ((j % R) == R - 1) {
                     short_batch |= (br.avail < 0) ? 1u : 0u;

@@ -11,8 +11,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "cg_internal.h"
 
 namespace {
@@ -20,30 +18,19 @@ namespace {
 // The shared scratch. Its size is CG_NOALLOC_SCRATCH_BYTES (cachegen.h).
 static __device__ __align__(256) uint8_t g_noalloc_scratch[CG_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch on the current device. In host code the
-// array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// Device address of the scratch in the current device's context. In host
+// code the array's name is only a host-side stand-in, so the address is
+// asked for on every call, with the caller's device current: nothing is
+// cached, so a context that was torn down and created again (a device
+// reset) can never leave a stale address behind. The first call in a
+// context also loads this file's device code there.
 cudaError_t scratch_address(void **out)
 {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (err != cudaSuccess)
         return err;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (err != cudaSuccess)
-            return err;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 

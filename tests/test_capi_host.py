@@ -264,3 +264,102 @@ def test_deserialize_objects_checks_headers_first(orc, lib):
             cg.cg_plan_destroy(plan2)
     finally:
         cg.cg_plan_destroy(plan)
+
+
+def test_plan_config_reports_the_configuration(orc):
+    """cg_plan_config gives back the shape and spec lists of a plan, also of
+    one opened from a container (from_bytes must recover them)."""
+    import torch
+    k = [(0, 3, 32), (3, 12, 16)]
+    v = [(0, 2, 32), (2, 5, 8), (5, 12, 16)]
+    plan = cg.cg_plan_create(12, 700, 12, 64, 128, k, v)
+    try:
+        assert cg.cg_plan_config(plan) == (12, 700, 12, 64, 128, k, v)
+        cfg = cg.cg_config()
+        ka = (cg.cg_quant_spec * 2)()
+        va = (cg.cg_quant_spec * 2)()   # one short: nothing is copied
+        lib = cg.load()
+        st = lib.cg_plan_config(ct.c_void_p(plan), ct.byref(cfg), ka, 2, va, 2)
+        assert st == cg.CG_ERR_CAPACITY
+        assert (cfg.n_kspecs, cfg.n_vspecs, cfg.num_tokens) == (2, 3, 700)
+        assert (va[0].start_layer, va[0].end_layer, va[0].bins) == (0, 0, 0)
+        assert lib.cg_plan_config(None, ct.byref(cfg), None, 0, None, 0) == cg.CG_ERR_INVALID_ARG
+        assert lib.cg_plan_config(ct.c_void_p(plan), ct.byref(cfg), None, 2, None, 0) == \
+            cg.CG_ERR_INVALID_ARG
+    finally:
+        cg.cg_plan_destroy(plan)
+    name = "glm4_9b_t32k"
+    kv = synthetic.generate(name, num_tokens=260)
+    L, _, T, C = kv.shape
+    ks, vs = synthetic.workload_specs(name)
+    enc = orc.encode(kv, 256, ks, vs)
+    blob = orc.serialize(enc, L, T, 2, 128, 256, ks, vs)
+    host = torch.from_numpy(np.frombuffer(blob, dtype=np.uint8).copy())
+    plan, _ = cg.cg_container_open(host)
+    try:
+        assert cg.cg_plan_config(plan) == (L, T, 2, 128, 256, [tuple(s) for s in ks],
+                                           [tuple(s) for s in vs])
+    finally:
+        cg.cg_plan_destroy(plan)
+
+
+def test_encode_decode_argument_checks(lib):
+    """cg_encode / cg_decode reject null and misaligned pointers and short
+    buffers before anything is enqueued (the fake addresses below are never
+    dereferenced: each call fails validation on the host)."""
+    plan = _plan(L=2, T=300, H=2, D=64, ch=256, k=[(0, 2, 16)], v=[(0, 2, 32)])
+    try:
+        s = cg.cg_plan_sizes(plan)
+        P = ct.c_void_p
+        base = 1 << 20   # 256-byte aligned fake address
+        ws = P(base)
+
+        def enc(bs=base, ln=base, cdf=base, am=base, cap=1 << 20):
+            return cg.cg_encoded(bs, cap, ln, cdf, am)
+
+        good = enc()
+        E = lambda kv, w, wb, e: lib.cg_encode(P(plan), kv, w, wb, ct.byref(e), None)  # noqa: E731
+        assert E(None, ws, s.workspace_bytes, good) == cg.CG_ERR_INVALID_ARG
+        assert E(P(base), None, s.workspace_bytes, good) == cg.CG_ERR_INVALID_ARG
+        assert lib.cg_encode(None, P(base), ws, s.workspace_bytes, ct.byref(good), None) == \
+            cg.CG_ERR_INVALID_ARG
+        assert lib.cg_encode(P(plan), P(base), ws, s.workspace_bytes, None, None) == \
+            cg.CG_ERR_INVALID_ARG
+        for bad in (enc(bs=0), enc(ln=0), enc(cdf=0), enc(am=0)):
+            assert E(P(base), ws, s.workspace_bytes, bad) == cg.CG_ERR_INVALID_ARG
+        assert E(P(base + 8), ws, s.workspace_bytes, good) == cg.CG_ERR_INVALID_ARG   # kv
+        assert E(P(base), P(base + 16), s.workspace_bytes, good) == cg.CG_ERR_INVALID_ARG
+        for bad in (enc(bs=base + 4), enc(cdf=base + 8), enc(ln=base + 2), enc(am=base + 1)):
+            assert E(P(base), ws, s.workspace_bytes, bad) == cg.CG_ERR_INVALID_ARG
+        assert E(P(base), ws, s.workspace_bytes - 1, good) == cg.CG_ERR_CAPACITY
+
+        n = s.num_streams
+        D = lambda e, sb, w, wb, out: lib.cg_decode(P(plan), ct.byref(e), sb, w, wb, out,  # noqa: E731
+                                                    None)
+        assert D(good, n, None, s.workspace_bytes, P(base)) == cg.CG_ERR_INVALID_ARG
+        assert D(good, n, ws, s.workspace_bytes, None) == cg.CG_ERR_INVALID_ARG
+        assert lib.cg_decode(P(plan), None, n, ws, s.workspace_bytes, P(base), None) == \
+            cg.CG_ERR_INVALID_ARG
+        for bad in (enc(bs=0), enc(ln=0), enc(cdf=0), enc(am=0), enc(bs=base + 4),
+                    enc(cdf=base + 2), enc(ln=base + 2), enc(am=base + 2)):
+            assert D(bad, n, ws, s.workspace_bytes, P(base)) == cg.CG_ERR_INVALID_ARG
+        assert D(good, n, ws, s.workspace_bytes, P(base + 8)) == cg.CG_ERR_INVALID_ARG
+        assert D(good, n, P(base + 128), s.workspace_bytes, P(base)) == cg.CG_ERR_INVALID_ARG
+        assert D(good, n - 1, ws, s.workspace_bytes, P(base)) == cg.CG_ERR_CORRUPT
+        assert D(enc(cap=n), n + 1, ws, s.workspace_bytes, P(base)) == cg.CG_ERR_CAPACITY
+        assert D(good, n, ws, 255, P(base)) == cg.CG_ERR_CAPACITY
+    finally:
+        cg.cg_plan_destroy(plan)
+
+
+def test_status_buffers_are_checked_before_the_call():
+    """The Python binding refuses a status buffer the C side would overrun
+    (the C side copies 16 bytes into it)."""
+    import torch
+    small = torch.zeros(8, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        cg.cg_encode_noalloc(0, small, small, small, small, small, small)
+    with pytest.raises(ValueError):
+        cg.cg_int8_encode(small, 1, 8, small, small, small)
+    with pytest.raises(ValueError):
+        cg.cg_int8_encode(small, 1, 8, small, small, None)
