@@ -256,6 +256,15 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
             delete p;
             return CG_ERR_UNSUPPORTED;
         }
+        // 16-bin symbols (at most 14) as 4-bit codes when the encoder's
+        // four-channels-per-thread path runs and rows stay 16-byte aligned
+        tp.nib_begin = tp.nib_end = 0;
+        if (C >= 4 * CG_TILE_THREADS && C % 32 == 0)
+            for (const cg_bin_class &cl : p->classes)
+                if (cl.bins == 16) {
+                    tp.nib_begin = cl.begin;
+                    tp.nib_end = cl.begin + cl.count;
+                }
     }
 
     // workspace: status | tile totals | tile bases | symbols | slots
@@ -265,7 +274,8 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
     p->ws_tile_base = w;
     w = align_up(w + 8 * ((size_t)ntiles + 1), 256);
     p->ws_symbols = w;
-    w = align_up(w + (size_t)p->num_streams * C, 256);
+    const size_t nib_pairs = (size_t)(tp.nib_end - tp.nib_begin);
+    w = align_up(w + (size_t)T * ((size_t)C * 2 * L - (size_t)(C / 2) * nib_pairs), 256);
     p->ws_slots = w;
     w = align_up(w + (size_t)p->num_streams * tp.slot_stride, 256);
     p->ws_bytes = w;

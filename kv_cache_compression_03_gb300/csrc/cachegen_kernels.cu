@@ -57,6 +57,7 @@ __device__ __forceinline__ void set_status(uint32_t *st, uint32_t code)
 struct Tile {
     int32_t index;  // (g * 2 + kv) * L + l
     int32_t g, kv, l, t0, n, N;
+    int32_t pair;   // position of (kv, l) in P.order (class launches), else -1
     uint64_t first_stream;  // index of the tile's first stream
     uint64_t cdf_base;      // entry offset of the tile's CDF block
 };
@@ -85,6 +86,7 @@ __device__ __forceinline__ Tile make_tile(const cg_tile_params &P, int32_t g, in
     t.N = P.bins[kv][l];
     t.first_stream = (uint64_t)2 * P.L * t.t0 + ((uint64_t)kv * P.L + l) * (uint64_t)t.n;
     t.cdf_base = (uint64_t)g * P.cdf_per_group + P.cdf_off[kv][l];
+    t.pair = -1;
     return t;
 }
 
@@ -95,7 +97,9 @@ __device__ __forceinline__ Tile tile_of_class(const cg_tile_params &P, int32_t b
     const int32_t i = b / P.ngroups;
     const int32_t g = b - i * P.ngroups;
     const uint32_t kvl = P.order[begin + i];
-    return make_tile(P, g, (int32_t)(kvl >> 8), (int32_t)(kvl & 0xFFu));
+    Tile t = make_tile(P, g, (int32_t)(kvl >> 8), (int32_t)(kvl & 0xFFu));
+    t.pair = begin + i;
+    return t;
 }
 
 // Tile by its global index (kernels that cover every tile).
@@ -382,7 +386,7 @@ __device__ __forceinline__ uint32_t enc_finish(Enc &e)
 // shared table. Returns the length in bits; *flag is set when the fast
 // path met a carry it cannot place (then the caller codes it again with
 // EXACT). Reads 16 symbols per load when C is a multiple of 16.
-template <bool EXACT>
+template <bool EXACT, bool NIB>
 __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
                                                 const uint16_t *table, int32_t Lp, uint32_t *out,
                                                 uint32_t cap, uint32_t *wp_out, uint32_t *flag)
@@ -398,7 +402,28 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
     e.flag = 0;
     e.out = out;
     const uint16_t *trow = table;
-    if ((C & 15) == 0) {
+    if (NIB) {
+        // 4-bit codes, 32 per 16-byte load (C is a multiple of 32): byte k
+        // of a word holds channels 2k (low half) and 2k + 1 (high half)
+        const uint4 *srow = reinterpret_cast<const uint4 *>(srow8);
+        uint4 next = srow[0];
+        for (int32_t c0 = 0; c0 < C; c0 += 32) {
+            const uint4 v = next;
+            if (c0 + 32 < C)
+                next = srow[(c0 >> 5) + 1];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint32_t word = (j < 8) ? v.x : (j < 16) ? v.y : (j < 24) ? v.z : v.w;
+                const uint32_t half = (j & 1) ? ((word >> 4) & 0x0F0F0F0Fu) : (word & 0x0F0F0F0Fu);
+                const uint32_t s = __byte_perm(half, 0, 0x4440 + ((j >> 1) & 3));
+                if (EXACT || (j % kStoreEvery) == kStoreEvery - 1)
+                    enc_symbol<EXACT, true>(e, trow[s], trow[s + 1]);
+                else
+                    enc_symbol<EXACT, false>(e, trow[s], trow[s + 1]);
+                trow += Lp;
+            }
+        }
+    } else if ((C & 15) == 0) {
         const uint4 *srow = reinterpret_cast<const uint4 *>(srow8);
         uint4 next = srow[0];
         for (int32_t c0 = 0; c0 < C; c0 += 16) {
@@ -444,19 +469,20 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
 
 // The exact path, kept out of line: it runs only for streams where the
 // fast path raised its flag. Returns (words << 32) | bits.
+template <bool NIB>
 __device__ __noinline__ uint64_t code_stream_exact(const uint8_t *srow8, int32_t C,
                                                    const uint16_t *table, int32_t Lp,
                                                    uint32_t *out, uint32_t cap)
 {
     uint32_t flag = 0, wp = 0;
-    const uint32_t bits = code_stream<true>(srow8, C, table, Lp, out, cap, &wp, &flag);
+    const uint32_t bits = code_stream<true, NIB>(srow8, C, table, Lp, out, cap, &wp, &flag);
     return ((uint64_t)wp << 32) | bits;
 }
 
 // Phase A, counting one block of rows: each thread owns W consecutive
 // channels (W = 4 with 8-byte loads and 4-byte symbol stores; W = 2 and 1
 // for narrower rows).
-template <int NB, int W>
+template <int NB, int W, bool NIB>
 __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, int32_t C,
                                             int32_t r0, int32_t nr, const float *fac, float fmax,
                                             uint16_t *table, int32_t N, uint8_t *sym_tile)
@@ -467,7 +493,39 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
         uint16_t *h0 = table + (size_t)(W * p) * Lp;
         for (int32_t rb = r0; rb < r0 + nr; rb += kCountBatch) {
             const int32_t nb = min(kCountBatch, r0 + nr - rb);
-            if (W == 4) {
+            if (W == 4 && nb == kCountBatch) {
+                // a full batch: no per-row predicates, addresses from one base
+                const uint2 *src = reinterpret_cast<const uint2 *>(rows) + p + (size_t)rb * (C / 4);
+                uint2 w[kCountBatch];
+#pragma unroll
+                for (int u = 0; u < kCountBatch; ++u)
+                    w[u] = __ldg(src + (size_t)u * (C / 4));
+#pragma unroll
+                for (int u = 0; u < kCountBatch; ++u) {
+                    const float f = fac[rb + u];
+                    const uint32_t b0 = quantise_bits(__uint_as_float(w[u].x << 16), f, fmax);
+                    const uint32_t b1 = quantise_bits(__uint_as_float(w[u].x & 0xFFFF0000u), f, fmax);
+                    const uint32_t b2 = quantise_bits(__uint_as_float(w[u].y << 16), f, fmax);
+                    const uint32_t b3 = quantise_bits(__uint_as_float(w[u].y & 0xFFFF0000u), f, fmax);
+                    const uint32_t q0 = symbol_of<NB>(b0, N), q1 = symbol_of<NB>(b1, N);
+                    const uint32_t q2 = symbol_of<NB>(b2, N), q3 = symbol_of<NB>(b3, N);
+                    h0[q0] += 1;
+                    h0[Lp + q1] += 1;
+                    h0[2 * Lp + q2] += 1;
+                    h0[3 * Lp + q3] += 1;
+                    if (NIB) {
+                        // four 4-bit codes, channel 4p + i in bits 4i..4i+3: the
+                        // sum of the raw sums' bits weighted by 16^i, taken mod
+                        // 2^16 (their high bits are multiples of 2^22 and drop
+                        // out; q < 16 leaves no carry between codes)
+                        reinterpret_cast<uint16_t *>(sym_tile)[p + (size_t)(rb + u) * (C / 4)] =
+                            (uint16_t)(b0 + 16u * b1 + 256u * b2 + 4096u * b3);
+                    } else {
+                        reinterpret_cast<uint32_t *>(sym_tile)[p + (size_t)(rb + u) * (C / 4)] =
+                            __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
+                    }
+                }
+            } else if (W == 4) {
                 const uint2 *src = reinterpret_cast<const uint2 *>(rows) + p;
                 uint32_t *dst = reinterpret_cast<uint32_t *>(sym_tile) + p;
                 uint2 w[kCountBatch];
@@ -486,8 +544,12 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
                         h0[Lp + q1] += 1;
                         h0[2 * Lp + q2] += 1;
                         h0[3 * Lp + q3] += 1;
-                        dst[(size_t)(rb + u) * (C / 4)] =
-                            __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
+                        if (NIB)
+                            reinterpret_cast<uint16_t *>(sym_tile)[p + (size_t)(rb + u) * (C / 4)] =
+                                (uint16_t)(q0 | (q1 << 4) | (q2 << 8) | (q3 << 12));
+                        else
+                            dst[(size_t)(rb + u) * (C / 4)] =
+                                __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
                     }
                 }
             } else if (W == 2) {
@@ -635,7 +697,14 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     __syncthreads();
     const uint16_t *rows = kv + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0) * (size_t)C;
     float *amax_row = amax_out + ((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0;
-    uint8_t *sym_tile = sym_ws + tl.first_stream * (uint64_t)C;
+    // symbol rows: the pair's region (T rows, pairs in the order of
+    // P.order, 4-bit codes for pairs in [nib_begin, nib_end)), then the
+    // group's rows from its first token
+    const bool nib = NB == 16 && tl.pair >= P.nib_begin && tl.pair < P.nib_end;
+    const uint32_t row_bytes = nib ? (uint32_t)C / 2 : (uint32_t)C;
+    const int32_t nib_before = min(max(tl.pair - P.nib_begin, 0), P.nib_end - P.nib_begin);
+    uint8_t *sym_tile = sym_ws + (uint64_t)P.T * ((uint64_t)C * tl.pair - (uint64_t)(C / 2) * nib_before) +
+                        (uint64_t)tl.t0 * row_bytes;
     const int32_t nblocks = (tl.n + kRowsPerBlock - 1) / kRowsPerBlock;
 
     // A: amax of block 0; then per step, count block b while the loads for
@@ -655,12 +724,14 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
         uint4 xa[4];
         if (pipelined)
             amax_issue(rows + (size_t)ta * C, C, ta < tl.n, xa);
-        if (C / 4 >= NT)
-            count_block<NB, 4>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+        if (nib)
+            count_block<NB, 4, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+        else if (C / 4 >= NT)
+            count_block<NB, 4, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
         else if (C / 2 >= NT)
-            count_block<NB, 2>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            count_block<NB, 2, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
         else
-            count_block<NB, 1>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            count_block<NB, 1, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
         if (pipelined)
             amax_finish(xa, ta < tl.n, fmax, &fac[ta], &amax_row[ta], nonfinite);
         else if (ta < tl.n)
@@ -705,13 +776,15 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     // C: one stream per token
     uint32_t nbytes_stream = 0;
     if (tid < tl.n) {
-        const uint8_t *srow = sym_tile + (size_t)tid * C;
+        const uint8_t *srow = sym_tile + (size_t)tid * row_bytes;
         uint32_t *out = reinterpret_cast<uint32_t *>(slots + (tl.first_stream + tid) * (uint64_t)P.slot_stride + 16);
         const uint32_t cap = (P.slot_stride - 16) / 4;
         uint32_t wp = 0, flag = 0;
-        uint32_t bits = code_stream<false>(srow, C, table, Lp, out, cap, &wp, &flag);
+        uint32_t bits = nib ? code_stream<false, true>(srow, C, table, Lp, out, cap, &wp, &flag)
+                            : code_stream<false, false>(srow, C, table, Lp, out, cap, &wp, &flag);
         if (flag) {
-            const uint64_t r = code_stream_exact(srow, C, table, Lp, out, cap);
+            const uint64_t r = nib ? code_stream_exact<true>(srow, C, table, Lp, out, cap)
+                                   : code_stream_exact<false>(srow, C, table, Lp, out, cap);
             bits = (uint32_t)r;
             wp = (uint32_t)(r >> 32);
         }
@@ -986,32 +1059,22 @@ __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's
-            // own comparison, so the result is exact), with r = d + 1 =
-            // 2^32 - e: r * c <= v * 2^16 + 0xFFFF  <=>  e * c + V >= c * 2^32
-            // for V = v * 2^16 + 0xFFFF, i.e. the high word of the 64-bit
-            // e * c + V is >= c (one wide multiply-add and one compare per
-            // probe; e fits 32 bits also when r = 2^32)
+            // own comparison, so the result is exact)
             // (sb = 2s, the position as a byte offset into the row: every
             // probe is then base + offset + constant)
             const char *rb = reinterpret_cast<const char *>(row);
-            const uint32_t e = ~d;
-            const uint64_t V = ((uint64_t)(v >> 16) << 32) | ((v << 16) | 0xFFFFu);
             uint32_t sb = 0;
             if (NB > 0 && (NB & (NB - 1)) == 0) {
 #pragma unroll
-                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1) {
-                    const uint32_t c = *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step);
-                    if ((uint32_t)(((uint64_t)e * c + V) >> 32) >= c)
+                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
+                    if (scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step)) <= v)
                         sb += 2 * step;
-                }
             } else {
                 for (uint32_t step = top_step; step != 0; step >>= 1) {
                     const uint32_t t = sb + 2 * step;
-                    if (t < 2 * (uint32_t)N) {
-                        const uint32_t c = *reinterpret_cast<const uint16_t *>(rb + t);
-                        if ((uint32_t)(((uint64_t)e * c + V) >> 32) >= c)
-                            sb = t;
-                    }
+                    if (t < 2 * (uint32_t)N &&
+                        scale16(d, *reinterpret_cast<const uint16_t *>(rb + t)) <= v)
+                        sb = t;
                 }
             }
             // sb <= 2(N - 1), so both bounds lie in the row. A valid stream

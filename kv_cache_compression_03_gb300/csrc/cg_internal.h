@@ -34,6 +34,11 @@ struct cg_tile_params {
     int32_t groups_per_object, full_objects;
     uint64_t cdf_per_group;  // CDF entries of one group (all K/V, layers)
     uint32_t slot_stride;    // bytes of one stream slot in the workspace (16-byte pad first)
+    // symbol scratch: the (kv, layer) pairs order[nib_begin, nib_end) (the
+    // 16-bin pairs, when C is a multiple of 32 and at least 1024) keep their
+    // symbols as 4-bit codes (C/2 bytes per token), all others as bytes; the
+    // pairs' regions follow the order of `order`, each T rows long
+    int32_t nib_begin, nib_end;
     uint32_t pad_;
     uint8_t bins[2][CG_MAX_LAYERS];
     uint32_t cdf_off[2][CG_MAX_LAYERS];  // offset of (kv, l) inside a group block
