@@ -514,12 +514,10 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
                     h0[2 * Lp + q2] += 1;
                     h0[3 * Lp + q3] += 1;
                     if (NIB) {
-                        // four 4-bit codes, channel 4p + i in bits 4i..4i+3: the
-                        // sum of the raw sums' bits weighted by 16^i, taken mod
-                        // 2^16 (their high bits are multiples of 2^22 and drop
-                        // out; q < 16 leaves no carry between codes)
+                        // four 4-bit codes, channel 4p + i in bits 4i..4i+3
+                        // (multiply-adds: q < 16 leaves no carry between codes)
                         reinterpret_cast<uint16_t *>(sym_tile)[p + (size_t)(rb + u) * (C / 4)] =
-                            (uint16_t)(b0 + 16u * b1 + 256u * b2 + 4096u * b3);
+                            (uint16_t)(q0 + 16u * q1 + 256u * q2 + 4096u * q3);
                     } else {
                         reinterpret_cast<uint32_t *>(sym_tile)[p + (size_t)(rb + u) * (C / 4)] =
                             __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
@@ -771,6 +769,17 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
         const uint4 *src = reinterpret_cast<const uint4 *>(table);
         for (uint32_t i = tid; i < nbytes / 16; i += NT)
             dst[i] = src[i];
+    }
+    if (*nonfinite) {
+        // inf/NaN values of a reported row quantise to the top symbol N - 1
+        // (symbol_of); its upper bound cdf[N] = 65536 is held as 0 in the
+        // table. Coding such a tile (its output is undefined) with 65535 as
+        // that bound keeps every interval well formed: the top symbol then
+        // occurs, so cdf[N - 1] <= 65534 and its width stays >= 1 of 2^16.
+        __syncthreads();
+        for (int32_t c = tid; c < C; c += NT)
+            table[(size_t)c * Lp + N] = 0xFFFFu;
+        __syncthreads();
     }
 
     // C: one stream per token

@@ -112,6 +112,11 @@ EDGE = [
     (2, 300, 2, 32, 256, [(0, 2, 64)], [(0, 2, 16)], "tiny"),       # amax near 2^-118
     (2, 512, 2, 64, 256, [(0, 2, 16)], [(0, 2, 32)], "sparse"),     # rows of rare symbols only
     (1, 256, 1, 64, 256, [(0, 1, 16)], [(0, 1, 16)], "sparse1"),    # one busy row per group
+    # C >= 1024 and a multiple of 32: 16-bin symbols kept as 4-bit codes
+    (2, 300, 8, 128, 256, [(0, 2, 16)], [(0, 2, 32)], "sparse"),    # 4-bit codes, exact re-code
+    (2, 256, 8, 128, 256, [(0, 2, 16)], [(0, 2, 16)], "bimodal"),   # 4-bit codes, carry runs
+    (1, 300, 8, 160, 256, [(0, 1, 16)], [(0, 1, 16)], "extreme"),   # C = 1280, ragged group
+    (1, 100, 3, 344, 256, [(0, 1, 16)], [(0, 1, 16)], "normal"),    # C = 1032: byte codes
 ]
 
 
@@ -211,6 +216,28 @@ def test_nonfinite_input_is_reported():
     st, total = cg.cg_last_device_error(codec.plan, codec.workspace)
     assert st == cg.CG_ERR_NONFINITE
     assert 0 < total <= codec.sizes.max_stream_bytes
+
+
+def test_nonfinite_rows_with_4bit_codes_are_reported():
+    # 1024-channel rows (16-bin symbols kept as 4-bit codes): a row of NaN,
+    # scattered infinities; the status is reported and every stream stays
+    # inside its bounds (the output itself is undefined)
+    name = "llama8b_t16k"
+    p = synthetic.WORKLOADS[name]
+    bits = synthetic.generate(name, num_tokens=300).copy()
+    bits[20, 0, 7, :] = 0x7FC0          # a whole K row of NaN (16 bins)
+    bits[20, 1, 260, ::97] = 0xFF80     # -inf in a V row (16 bins)
+    bits[1, 0, 3, 5] = 0x7F80           # +inf in a 32-bin row
+    k, v = synthetic.workload_specs(name)
+    L, _, T, C = bits.shape
+    codec = cg.Codec(L, T, p["H"], p["D"], 256, k, v)
+    enc = codec.alloc_encoded()
+    cg.cg_encode(codec.plan, _to_dev(bits, p["H"], p["D"]), codec.workspace, enc.bytestream,
+                 enc.lengths, enc.cdf, enc.amax)
+    st, total = cg.cg_last_device_error(codec.plan, codec.workspace)
+    assert st == cg.CG_ERR_NONFINITE
+    lengths = enc.lengths.cpu().numpy()
+    assert lengths.min() >= 1 and lengths.max() <= 3 * C
 
 
 def test_tiny_row_is_reported():
