@@ -1046,18 +1046,33 @@ constexpr int kRefillEvery = 4;
 // caller decodes the stream again with R = 1, which never runs short: a
 // symbol takes at most 18 bits and the buffer holds at least 33 after every
 // refill).
+// Decoder state: x = window of the absolute low end, d = range - 1,
+// v = code value - low end, and the bit reader.
+struct DecState {
+    uint32_t x, d, v;
+    Bits br;
+};
+
+__device__ __forceinline__ void dec_start(DecState &st, const Bits &br)
+{
+    st.x = 0;
+    st.d = 0xFFFFFFFFu;
+    st.v = br.b1;
+    st.br = br;
+    bits_skip(st.br, 16);
+    bits_skip(st.br, 16);
+}
+
+// Decode the next C symbols of a stream with the CDF rows of `table` (row c
+// for the c-th of them) and write their dequantised values to orow[0, C).
 template <int NB, int R>
-__device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t C, int32_t N,
-                                                  Bits br, float a, const float *deq,
-                                                  uint16_t *orow)
+__device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t *table, int32_t C,
+                                                   int32_t N, float a, const float *deq,
+                                                   uint16_t *orow)
 {
     const int32_t Lp = N + 1;
-    // state: x = window of the absolute low end, d = range - 1,
-    // v = code value - low end
-    uint32_t x = 0, d = 0xFFFFFFFFu;
-    uint32_t v = br.b1;
-    bits_skip(br, 16);
-    bits_skip(br, 16);
+    uint32_t x = st.x, d = st.d, v = st.v;
+    Bits br = st.br;
     const uint16_t *row = table;
     const uint32_t top_step = 1u << (31 - __clz((uint32_t)(N - 1)));
     uint32_t short_batch = 0;
@@ -1126,7 +1141,26 @@ __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t
         *reinterpret_cast<uint4 *>(orow + c0) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
+    st.x = x;
+    st.d = d;
+    st.v = v;
+    st.br = br;
     return short_batch;
+}
+
+// Decode one stream (C symbols) and write its dequantised row. R > 1
+// refills the bit buffer once per R symbols and returns 1 when a batch ran
+// short of bits (the output is then wrong and the caller decodes the stream
+// again with R = 1, which never runs short: a symbol takes at most 18 bits
+// and the buffer holds at least 33 after every refill).
+template <int NB, int R>
+__device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t C, int32_t N,
+                                                  const Bits &br, float a, const float *deq,
+                                                  uint16_t *orow)
+{
+    DecState st;
+    dec_start(st, br);
+    return decode_symbols<NB, R>(st, table, C, N, a, deq, orow);
 }
 
 // The refill-per-symbol decode of one stream, out of line: it runs only for
@@ -1140,6 +1174,18 @@ __device__ __noinline__ void decode_stream_exact(const uint16_t *table, int32_t 
     Bits br;
     bits_init(br, bytestream, sb, last);
     decode_stream<NB, 1>(table, C, N, br, a, deq, orow);
+}
+
+// The same for the symbols of one channel part, from the state `st` held
+// at the part's start (updated to the state after the part).
+template <int NB>
+__device__ __noinline__ void decode_part_exact(DecState *st, const uint16_t *table, int32_t C,
+                                               int32_t N, float a, const float *deq,
+                                               uint16_t *orow)
+{
+    DecState s = *st;
+    decode_symbols<NB, 1>(s, table, C, N, a, deq, orow);
+    *st = s;
 }
 
 // One tile of the decoder; NB as in encode_tile.
@@ -1213,23 +1259,116 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
         decode_stream_exact<NB>(table, C, N, bytestream, sb, last, a, deq, orow);
 }
 
+// One tile of the decoder whose CDF table is staged in channel parts of
+// part_ch channels (a multiple of 8): tables too large for several CTAs per
+// SM (32 and 64 bins at 1024 channels, 16 bins at 4096) take the shared
+// memory of one part. Every stream decodes a part's channels, its coder state
+// staying in registers; a block barrier separates the parts. A stream whose
+// batched decode of a part ran short of bits decodes that part again, from
+// the state it held at the part's start, refilling after every symbol.
+template <int NB>
+__device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_params &P,
+                                                  const uint8_t *__restrict__ bytestream,
+                                                  uint64_t stream_bytes,
+                                                  const int32_t *__restrict__ lengths,
+                                                  const uint16_t *__restrict__ cdf,
+                                                  const float *__restrict__ amax,
+                                                  const uint64_t *__restrict__ tile_base,
+                                                  uint16_t *__restrict__ kv_out,
+                                                  uint32_t *__restrict__ status, uint8_t *smem,
+                                                  uint32_t *warp_sums, float *deq, uint32_t *bad,
+                                                  int32_t part_ch)
+{
+    const int32_t C = P.C;
+    const int32_t N = NB > 0 ? NB : tl.N;
+    const int32_t Lp = N + 1;
+    const int32_t M = N / 2 - 1;
+    const int tid = threadIdx.x;
+    uint16_t *table = reinterpret_cast<uint16_t *>(smem);
+
+    if (tid == 0)
+        *bad = 0;
+    if (tid < N)
+        deq[tid] = __fdiv_rn((float)(tid - M), (float)M);
+    uint32_t len = 0;
+    const bool active = tid < tl.n;
+    if (active) {
+        const int32_t v = lengths[tl.first_stream + tid];
+        len = (v > 0) ? (uint32_t)v : 0u;
+    }
+    const uint32_t off = block_exclusive_scan(len, warp_sums, nullptr);  // has __syncthreads
+    DecState st;
+    float a = 0.0f;
+    uint16_t *orow = kv_out;
+    if (active) {
+        const uint64_t last = ((stream_bytes + 3) & ~(uint64_t)3) - 4;
+        uint64_t sb = tile_base[tl.index] + off;
+        if (sb + len > stream_bytes) {
+            set_status(status, CG_ERR_CORRUPT);
+            sb = min(sb, last);
+        }
+        a = amax[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + tid];
+        orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + tid) * (size_t)C;
+        Bits br;
+        bits_init(br, bytestream, sb, last);
+        dec_start(st, br);
+    }
+    for (int32_t c_begin = 0; c_begin < C; c_begin += part_ch) {
+        const int32_t nch = min(part_ch, C - c_begin);
+        {
+            const uint32_t nb16 = (uint32_t)nch * Lp * 2u / 16u;
+            const uint4 *src = reinterpret_cast<const uint4 *>(cdf + tl.cdf_base + (size_t)c_begin * Lp);
+            uint4 *dst = reinterpret_cast<uint4 *>(table);
+            for (uint32_t i = tid; i < nb16; i += NT)
+                dst[i] = __ldg(src + i);
+        }
+        __syncthreads();
+        for (int32_t c = tid; c < nch; c += NT) {
+            const uint16_t *row = table + (size_t)c * Lp;
+            uint32_t ok = (row[0] == 0) && (row[N] == 0);
+            for (int32_t i = 1; i < N; ++i)
+                ok &= (row[i] > row[i - 1]) ? 1u : 0u;
+            if (!ok)
+                *bad = 1;
+        }
+        __syncthreads();
+        if (*bad) {
+            if (tid == 0)
+                set_status(status, CG_ERR_CORRUPT);
+            return;
+        }
+        if (active) {
+            const DecState saved = st;
+            if (decode_symbols<NB, kRefillEvery>(st, table, nch, N, a, deq, orow + c_begin)) {
+                st = saved;
+                decode_part_exact<NB>(&st, table, nch, N, a, deq, orow + c_begin);
+            }
+        }
+        __syncthreads();  // the next part overwrites the table
+    }
+}
+
 // Decoder tiles of one launch class (NB bins; 0 = any), at least MINB
-// CTAs per SM.
-template <int NB, int MINB>
+// CTAs per SM; PARTS: the CDF table is staged in parts of part_ch channels.
+template <int NB, int MINB, bool PARTS>
 __global__ void __launch_bounds__(NT, MINB)
     k_decode_class(const cg_tile_params P, int32_t cls_begin,
                    const uint8_t *__restrict__ bytestream, uint64_t stream_bytes,
                    const int32_t *__restrict__ lengths, const uint16_t *__restrict__ cdf,
                    const float *__restrict__ amax, const uint64_t *__restrict__ tile_base,
-                   uint16_t *__restrict__ kv_out, uint32_t *__restrict__ status)
+                   uint16_t *__restrict__ kv_out, uint32_t *__restrict__ status, int32_t part_ch)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t warp_sums[NT / 32];
     __shared__ float deq[64];
     __shared__ uint32_t bad;
     const Tile tl = tile_of_class(P, cls_begin, blockIdx.x);
-    decode_tile<NB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
-                    status, smem, warp_sums, deq, &bad);
+    if (PARTS)
+        decode_tile_parts<NB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
+                              kv_out, status, smem, warp_sums, deq, &bad, part_ch);
+    else
+        decode_tile<NB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
+                        status, smem, warp_sums, deq, &bad);
 }
 
 // The kernel of each class, by bin count: 16 and 32 have specialised
@@ -1238,7 +1377,7 @@ typedef void (*encode_fn)(const uint16_t *, const cg_tile_params, int32_t, uint8
                           uint16_t *, int32_t *, uint8_t *, uint32_t *, uint32_t *);
 typedef void (*decode_fn)(const cg_tile_params, int32_t, const uint8_t *, uint64_t,
                           const int32_t *, const uint16_t *, const float *, const uint64_t *,
-                          uint16_t *, uint32_t *);
+                          uint16_t *, uint32_t *, int32_t);
 
 encode_fn encode_kernel(int32_t bins)
 {
@@ -1249,13 +1388,13 @@ encode_fn encode_kernel(int32_t bins)
     return k_encode_class<0, 3>;
 }
 
-decode_fn decode_kernel(int32_t bins)
+decode_fn decode_kernel(int32_t bins, bool parts)
 {
     if (bins == 16)
-        return k_decode_class<16, 6>;
+        return parts ? k_decode_class<16, 4, true> : k_decode_class<16, 6, false>;
     if (bins == 32)
-        return k_decode_class<32, 3>;
-    return k_decode_class<0, 3>;
+        return parts ? k_decode_class<32, 4, true> : k_decode_class<32, 3, false>;
+    return parts ? k_decode_class<0, 4, true> : k_decode_class<0, 3, false>;
 }
 
 // The dynamic shared-memory limit is a per-device function attribute: set
@@ -1275,8 +1414,8 @@ cudaError_t ensure_smem_attributes()
         err = cudaFuncSetAttribute(encode_kernel(bins[i]),
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    CG_SMEM_LIMIT - 1024);
-        if (err == cudaSuccess)
-            err = cudaFuncSetAttribute(decode_kernel(bins[i]),
+        for (int parts = 0; parts < 2 && err == cudaSuccess; ++parts)
+            err = cudaFuncSetAttribute(decode_kernel(bins[i], parts != 0),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        CG_SMEM_LIMIT - 1024);
     }
@@ -1292,9 +1431,18 @@ size_t cg_smem_encode(int32_t C, int32_t bins)
     return (((size_t)C * (bins + 1) * 2 + 15) & ~(size_t)15) + CG_GROUP_TOKENS * sizeof(float);
 }
 
+int32_t cg_decode_part_channels(int32_t C, int32_t bins)
+{
+    const size_t table = (size_t)C * (bins + 1) * 2;
+    if (table <= CG_DECODE_TABLE_BUDGET)
+        return C;
+    const int32_t parts = (int32_t)((table + CG_DECODE_TABLE_BUDGET - 1) / CG_DECODE_TABLE_BUDGET);
+    return ((C + parts - 1) / parts + 7) / 8 * 8;
+}
+
 size_t cg_smem_decode(int32_t C, int32_t bins)
 {
-    return ((size_t)C * (bins + 1) * 2 + 15) & ~(size_t)15;
+    return ((size_t)cg_decode_part_channels(C, bins) * (bins + 1) * 2 + 15) & ~(size_t)15;
 }
 
 const char *cg_kernel_name(int id)
@@ -1459,9 +1607,10 @@ cudaError_t cg_launch_decode(const cg_plan *p, const cg_encoded *in, uint64_t st
     p->prof.end(stream);
     p->prof.begin(CG_K_DECODE_TILES, stream);
     err = launch_classes(p, stream, [&](const cg_bin_class &cl, cudaStream_t s) {
-        decode_kernel(cl.bins)<<<p->tp.ngroups * cl.count, NT, cl.smem_decode, s>>>(
+        const int32_t part_ch = cg_decode_part_channels(p->C, cl.bins);
+        decode_kernel(cl.bins, part_ch < p->C)<<<p->tp.ngroups * cl.count, NT, cl.smem_decode, s>>>(
             p->tp, cl.begin, in->bytestream, stream_bytes, in->lengths, in->cdf, in->amax,
-            tile_base, static_cast<uint16_t *>(kv_out), status);
+            tile_base, static_cast<uint16_t *>(kv_out), status, part_ch);
     });
     p->prof.end(stream);
     if (err != cudaSuccess)

@@ -114,3 +114,7 @@ int cg_decode_launch_count(const cg_plan *p);
 // dynamic shared memory of the tile kernels for C channels and `bins` bins
 size_t cg_smem_encode(int32_t C, int32_t bins);
 size_t cg_smem_decode(int32_t C, int32_t bins);
+// Decoder CDF tables above this many bytes are staged in channel parts so
+// that several CTAs fit on an SM; channels per part (C when one part).
+#define CG_DECODE_TABLE_BUDGET (36 * 1024)
+int32_t cg_decode_part_channels(int32_t C, int32_t bins);

@@ -312,13 +312,16 @@ def test_corrupt_containers_are_reported(orc):
     assert decode_status(base, sb=base.stream_bytes - 16)[0] == cg.CG_ERR_CORRUPT
 
 
-def test_decoder_batches_that_run_short(orc):
+@pytest.mark.parametrize("H,D,N", [(1, 32, 16), (8, 128, 32), (8, 128, 64)])
+def test_decoder_batches_that_run_short(orc, H, D, N):
     """The decoder refills its bit buffer once per few symbols; a run of
     symbols of frequency 1/65536 (which this encoder never produces, but a
     valid container may hold) takes ~16 bits each, so such a batch runs short
-    and the stream is decoded again exactly. Built by hand: CDF rows with two
-    frequency-1 symbols, streams coded by the oracle's coder."""
-    L, T, H, D, N = 1, 64, 1, 32, 16
+    and the stream (or, where the CDF table is staged in channel parts: 32
+    and 64 bins at 1024 channels, that part) is decoded again exactly. Built
+    by hand: CDF rows with two frequency-1 symbols, streams coded by the
+    oracle's coder."""
+    L, T = 1, 64
     C = H * D
     rng = np.random.default_rng(77)
     row = np.zeros(N + 1, dtype=np.int64)
