@@ -588,10 +588,15 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
     }
 }
 
-// Phase A, amax of one row (one warp): writes the factor, the scale and
-// raises the non-finite flag.
-__device__ __forceinline__ void row_amax(const uint16_t *__restrict__ row, int32_t C, float fmax,
-                                         float *fac_t, float *amax_t, uint32_t *nonfinite)
+// Phase A, largest |x| of one row (one warp) as bf16 bits, in every lane:
+// the lanes' maxima over the bf16 bit patterns with the sign cleared
+// (finite values order like their patterns), then one warp reduction.
+__device__ __forceinline__ uint32_t absmax_reduce(uint32_t m)
+{
+    return __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+}
+
+__device__ __forceinline__ uint32_t row_absmax(const uint16_t *__restrict__ row, int32_t C)
 {
     const int lane = threadIdx.x & 31;
     const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
@@ -603,14 +608,7 @@ __device__ __forceinline__ void row_amax(const uint16_t *__restrict__ row, int32
         m = __vmaxu2(m, x.z & 0x7FFF7FFFu);
         m = __vmaxu2(m, x.w & 0x7FFF7FFFu);
     }
-    m = max(m & 0xFFFFu, m >> 16);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) {
-        *fac_t = row_factor(m, fmax, nonfinite);
-        *amax_t = __uint_as_float(m << 16);
-    }
+    return absmax_reduce(m);
 }
 
 // Phase A, amax of one row in two halves: amax_issue starts the row's
@@ -628,8 +626,7 @@ __device__ __forceinline__ void amax_issue(const uint16_t *__restrict__ row, int
     }
 }
 
-__device__ __forceinline__ void amax_finish(const uint4 (&x)[4], bool valid, float fmax,
-                                            float *fac_t, float *amax_t, uint32_t *nonfinite)
+__device__ __forceinline__ uint32_t amax_finish(const uint4 (&x)[4])
 {
     uint32_t m = 0;
 #pragma unroll
@@ -639,13 +636,22 @@ __device__ __forceinline__ void amax_finish(const uint4 (&x)[4], bool valid, flo
         m = __vmaxu2(m, x[i].z & 0x7FFF7FFFu);
         m = __vmaxu2(m, x[i].w & 0x7FFF7FFFu);
     }
-    m = max(m & 0xFFFFu, m >> 16);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (valid && (threadIdx.x & 31) == 0) {
-        *fac_t = row_factor(m, fmax, nonfinite);
-        *amax_t = __uint_as_float(m << 16);
+    return absmax_reduce(m);
+}
+
+// The scale and factor of two rows a warp has reduced (rows ra and rb with
+// maxima ma and mb, in every lane): lane 0 takes ra and lane 1 rb, so the
+// two divisions run as one instruction sequence.
+__device__ __forceinline__ void store_factors(int32_t ra, uint32_t ma, int32_t rb, uint32_t mb,
+                                              int32_t n, float fmax, float *fac, float *amax_row,
+                                              uint32_t *nonfinite)
+{
+    const int lane = threadIdx.x & 31;
+    const int32_t r = lane ? rb : ra;
+    const uint32_t m = lane ? mb : ma;
+    if (lane < 2 && r < n) {
+        fac[r] = row_factor(m, fmax, nonfinite);
+        amax_row[r] = __uint_as_float(m << 16);
     }
 }
 
@@ -708,9 +714,13 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     // A: amax of block 0; then per step, count block b while the loads for
     // block b + 1's amax are in flight (one row per warp), and ask L2 for
     // block b + 2
-    for (int32_t rr = warp; rr < kRowsPerBlock; rr += NT / 32)
-        if (rr < tl.n)
-            row_amax(rows + (size_t)rr * C, C, fmax, &fac[rr], &amax_row[rr], nonfinite);
+    {
+        // rows warp and warp + 8 of block 0
+        const int32_t ra = warp, rb = warp + NT / 32;
+        const uint32_t ma = (ra < tl.n) ? row_absmax(rows + (size_t)ra * C, C) : 0u;
+        const uint32_t mb = (rb < tl.n) ? row_absmax(rows + (size_t)rb * C, C) : 0u;
+        store_factors(ra, ma, rb, mb, tl.n, fmax, fac, amax_row, nonfinite);
+    }
     __syncthreads();
     const bool pipelined = (C <= 1024);
     for (int32_t b = 0; b < nblocks; ++b) {
@@ -730,13 +740,11 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
             count_block<NB, 2, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
         else
             count_block<NB, 1, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
-        if (pipelined)
-            amax_finish(xa, ta < tl.n, fmax, &fac[ta], &amax_row[ta], nonfinite);
-        else if (ta < tl.n)
-            row_amax(rows + (size_t)ta * C, C, fmax, &fac[ta], &amax_row[ta], nonfinite);
+        const uint32_t ma = pipelined ? amax_finish(xa)
+                                      : (ta < tl.n) ? row_absmax(rows + (size_t)ta * C, C) : 0u;
         const int32_t tb = ta + NT / 32;
-        if (tb < tl.n)
-            row_amax(rows + (size_t)tb * C, C, fmax, &fac[tb], &amax_row[tb], nonfinite);
+        const uint32_t mb = (tb < tl.n) ? row_absmax(rows + (size_t)tb * C, C) : 0u;
+        store_factors(ta, ma, tb, mb, tl.n, fmax, fac, amax_row, nonfinite);
         __syncthreads();
     }
     if (tid == 0 && *nonfinite)
