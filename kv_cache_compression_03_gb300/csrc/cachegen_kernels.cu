@@ -108,7 +108,9 @@ __device__ __forceinline__ Tile tile_by_index(const cg_tile_params &P, int32_t i
     return make_tile(P, index / (2 * P.L), (index / P.L) & 1, index % P.L);
 }
 
-// Block-wide exclusive scan of one value per thread (256 threads).
+// Block-wide exclusive scan of one value per thread (NTH threads, a
+// multiple of 32 up to 1024).
+template <int NTH = NT>
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *warp_sums,
                                                          uint32_t *total)
 {
@@ -124,21 +126,68 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
         warp_sums[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = (lane < NT / 32) ? warp_sums[lane] : 0u;
+        uint32_t w = (lane < NTH / 32) ? warp_sums[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
             if (lane >= o)
                 w += y;
         }
-        if (lane < NT / 32)
+        if (lane < NTH / 32)
             warp_sums[lane] = w;  // inclusive
     }
     __syncthreads();
     const uint32_t before = (warp > 0) ? warp_sums[warp - 1] : 0u;
     if (total)
-        *total = warp_sums[NT / 32 - 1];
+        *total = warp_sums[NTH / 32 - 1];
     return before + x - v;
+}
+
+// The length (clamped at 0) and the byte offset within its tile of the
+// stream a decoder thread takes: stream h * NTH + threadIdx.x, the tile's
+// streams being split over NT / NTH CTAs of NTH threads. With NTH < NT each
+// thread scans NT / NTH consecutive lengths and the offsets go through
+// shared memory (offs, NT entries).
+template <int NTH>
+__device__ __forceinline__ uint32_t tile_stream_offset(const Tile &tl,
+                                                       const int32_t *__restrict__ lengths,
+                                                       int32_t h, uint32_t *len_out,
+                                                       uint32_t *warp_sums, uint32_t *offs)
+{
+    const int tid = threadIdx.x;
+    if (NTH == NT) {
+        uint32_t len = 0;
+        if (tid < tl.n) {
+            const int32_t v = lengths[tl.first_stream + tid];
+            len = (v > 0) ? (uint32_t)v : 0u;
+        }
+        *len_out = len;
+        return block_exclusive_scan<NT>(len, warp_sums, nullptr);  // has __syncthreads
+    }
+    constexpr int K = NT / NTH;
+    uint32_t l[K], sum = 0;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const int32_t sidx = tid * K + j;
+        const int32_t v = (sidx < tl.n) ? lengths[tl.first_stream + sidx] : 0;
+        l[j] = (v > 0) ? (uint32_t)v : 0u;
+        sum += l[j];
+    }
+    uint32_t base = block_exclusive_scan<NTH>(sum, warp_sums, nullptr);
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        offs[tid * K + j] = base;
+        base += l[j];
+    }
+    __syncthreads();
+    const int32_t sidx = h * NTH + tid;
+    uint32_t len = 0;
+    if (sidx < tl.n) {
+        const int32_t v = lengths[tl.first_stream + sidx];
+        len = (v > 0) ? (uint32_t)v : 0u;
+    }
+    *len_out = len;
+    return offs[sidx];
 }
 
 // ------------------------------------------------------------ quantiser
@@ -1196,8 +1245,9 @@ __device__ __noinline__ void decode_part_exact(DecState *st, const uint16_t *tab
     *st = s;
 }
 
-// One tile of the decoder; NB as in encode_tile.
-template <int NB>
+// One tile of the decoder; NB as in encode_tile. The CTA takes streams
+// [h * NTH, (h + 1) * NTH) of the tile.
+template <int NB, int NTH>
 __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params &P,
                                             const uint8_t *__restrict__ bytestream,
                                             uint64_t stream_bytes,
@@ -1207,13 +1257,15 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
                                             const uint64_t *__restrict__ tile_base,
                                             uint16_t *__restrict__ kv_out,
                                             uint32_t *__restrict__ status, uint8_t *smem,
-                                            uint32_t *warp_sums, float *deq, uint32_t *bad)
+                                            uint32_t *warp_sums, float *deq, uint32_t *bad,
+                                            int32_t h, uint32_t *offs)
 {
     const int32_t C = P.C;
     const int32_t N = NB > 0 ? NB : tl.N;
     const int32_t Lp = N + 1;
     const int32_t M = N / 2 - 1;
     const int tid = threadIdx.x;
+    const int32_t sidx = h * NTH + tid;
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
 
     if (tid == 0)
@@ -1222,19 +1274,15 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
         const uint32_t nb16 = (uint32_t)C * Lp * 2u / 16u;
         const uint4 *src = reinterpret_cast<const uint4 *>(cdf + tl.cdf_base);
         uint4 *dst = reinterpret_cast<uint4 *>(table);
-        for (uint32_t i = tid; i < nb16; i += NT)
+        for (uint32_t i = tid; i < nb16; i += NTH)
             dst[i] = __ldg(src + i);
     }
     if (tid < N)
         deq[tid] = __fdiv_rn((float)(tid - M), (float)M);
     uint32_t len = 0;
-    if (tid < tl.n) {
-        const int32_t v = lengths[tl.first_stream + tid];
-        len = (v > 0) ? (uint32_t)v : 0u;
-    }
-    const uint32_t off = block_exclusive_scan(len, warp_sums, nullptr);  // has __syncthreads
+    const uint32_t off = tile_stream_offset<NTH>(tl, lengths, h, &len, warp_sums, offs);
     // every row must start at 0, rise strictly and end at 65536 (stored 0)
-    for (int32_t c = tid; c < C; c += NT) {
+    for (int32_t c = tid; c < C; c += NTH) {
         const uint16_t *row = table + (size_t)c * Lp;
         uint32_t ok = (row[0] == 0) && (row[N] == 0);
         for (int32_t i = 1; i < N; ++i)
@@ -1248,7 +1296,7 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
             set_status(status, CG_ERR_CORRUPT);
         return;
     }
-    if (tid >= tl.n)
+    if (sidx >= tl.n)
         return;
 
     // the buffer holds stream_bytes (>= 1) bytes, rounded up to 16 (checked
@@ -1259,8 +1307,8 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
         set_status(status, CG_ERR_CORRUPT);
         sb = min(sb, last);
     }
-    const float a = amax[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + tid];
-    uint16_t *orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + tid) * (size_t)C;
+    const float a = amax[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + sidx];
+    uint16_t *orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + sidx) * (size_t)C;
     Bits br;
     bits_init(br, bytestream, sb, last);
     if (decode_stream<NB, kRefillEvery>(table, C, N, br, a, deq, orow))
@@ -1274,7 +1322,7 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
 // staying in registers; a block barrier separates the parts. A stream whose
 // batched decode of a part ran short of bits decodes that part again, from
 // the state it held at the part's start, refilling after every symbol.
-template <int NB>
+template <int NB, int NTH>
 __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_params &P,
                                                   const uint8_t *__restrict__ bytestream,
                                                   uint64_t stream_bytes,
@@ -1285,13 +1333,14 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
                                                   uint16_t *__restrict__ kv_out,
                                                   uint32_t *__restrict__ status, uint8_t *smem,
                                                   uint32_t *warp_sums, float *deq, uint32_t *bad,
-                                                  int32_t part_ch)
+                                                  int32_t part_ch, int32_t h, uint32_t *offs)
 {
     const int32_t C = P.C;
     const int32_t N = NB > 0 ? NB : tl.N;
     const int32_t Lp = N + 1;
     const int32_t M = N / 2 - 1;
     const int tid = threadIdx.x;
+    const int32_t sidx = h * NTH + tid;
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
 
     if (tid == 0)
@@ -1299,12 +1348,8 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
     if (tid < N)
         deq[tid] = __fdiv_rn((float)(tid - M), (float)M);
     uint32_t len = 0;
-    const bool active = tid < tl.n;
-    if (active) {
-        const int32_t v = lengths[tl.first_stream + tid];
-        len = (v > 0) ? (uint32_t)v : 0u;
-    }
-    const uint32_t off = block_exclusive_scan(len, warp_sums, nullptr);  // has __syncthreads
+    const bool active = sidx < tl.n;
+    const uint32_t off = tile_stream_offset<NTH>(tl, lengths, h, &len, warp_sums, offs);
     DecState st;
     float a = 0.0f;
     uint16_t *orow = kv_out;
@@ -1315,8 +1360,8 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
             set_status(status, CG_ERR_CORRUPT);
             sb = min(sb, last);
         }
-        a = amax[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + tid];
-        orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + tid) * (size_t)C;
+        a = amax[((size_t)tl.kv * P.L + tl.l) * P.T + tl.t0 + sidx];
+        orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + sidx) * (size_t)C;
         Bits br;
         bits_init(br, bytestream, sb, last);
         dec_start(st, br);
@@ -1327,11 +1372,11 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
             const uint32_t nb16 = (uint32_t)nch * Lp * 2u / 16u;
             const uint4 *src = reinterpret_cast<const uint4 *>(cdf + tl.cdf_base + (size_t)c_begin * Lp);
             uint4 *dst = reinterpret_cast<uint4 *>(table);
-            for (uint32_t i = tid; i < nb16; i += NT)
+            for (uint32_t i = tid; i < nb16; i += NTH)
                 dst[i] = __ldg(src + i);
         }
         __syncthreads();
-        for (int32_t c = tid; c < nch; c += NT) {
+        for (int32_t c = tid; c < nch; c += NTH) {
             const uint16_t *row = table + (size_t)c * Lp;
             uint32_t ok = (row[0] == 0) && (row[N] == 0);
             for (int32_t i = 1; i < N; ++i)
@@ -1357,9 +1402,11 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
 }
 
 // Decoder tiles of one launch class (NB bins; 0 = any), at least MINB
-// CTAs per SM; PARTS: the CDF table is staged in parts of part_ch channels.
-template <int NB, int MINB, bool PARTS>
-__global__ void __launch_bounds__(NT, MINB)
+// 256-thread CTAs' worth per SM; PARTS: the CDF table is staged in parts of
+// part_ch channels; NTH < 256: each tile's streams are split over 256 / NTH
+// CTAs of NTH threads (for calls with too few tiles to fill the GPU).
+template <int NB, int MINB, bool PARTS, int NTH>
+__global__ void __launch_bounds__(NTH, MINB *(NT / NTH))
     k_decode_class(const cg_tile_params P, int32_t cls_begin,
                    const uint8_t *__restrict__ bytestream, uint64_t stream_bytes,
                    const int32_t *__restrict__ lengths, const uint16_t *__restrict__ cdf,
@@ -1367,16 +1414,19 @@ __global__ void __launch_bounds__(NT, MINB)
                    uint16_t *__restrict__ kv_out, uint32_t *__restrict__ status, int32_t part_ch)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ uint32_t warp_sums[NT / 32];
+    __shared__ uint32_t warp_sums[NTH / 32];
     __shared__ float deq[64];
     __shared__ uint32_t bad;
-    const Tile tl = tile_of_class(P, cls_begin, blockIdx.x);
+    __shared__ uint32_t offs[NTH < NT ? NT : 1];
+    constexpr int split = NT / NTH;
+    const Tile tl = tile_of_class(P, cls_begin, blockIdx.x / split);
+    const int32_t h = (int32_t)(blockIdx.x % split);
     if (PARTS)
-        decode_tile_parts<NB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
-                              kv_out, status, smem, warp_sums, deq, &bad, part_ch);
+        decode_tile_parts<NB, NTH>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
+                                   kv_out, status, smem, warp_sums, deq, &bad, part_ch, h, offs);
     else
-        decode_tile<NB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base, kv_out,
-                        status, smem, warp_sums, deq, &bad);
+        decode_tile<NB, NTH>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
+                             kv_out, status, smem, warp_sums, deq, &bad, h, offs);
 }
 
 // The kernel of each class, by bin count: 16 and 32 have specialised
@@ -1396,13 +1446,35 @@ encode_fn encode_kernel(int32_t bins)
     return k_encode_class<0, 3>;
 }
 
-decode_fn decode_kernel(int32_t bins, bool parts)
+template <int NTH>
+decode_fn decode_kernel_nth(int32_t bins, bool parts)
 {
     if (bins == 16)
-        return parts ? k_decode_class<16, 4, true> : k_decode_class<16, 6, false>;
+        return parts ? k_decode_class<16, 4, true, NTH>
+                     : k_decode_class<16, (NTH == NT ? 6 : 4), false, NTH>;
     if (bins == 32)
-        return parts ? k_decode_class<32, 4, true> : k_decode_class<32, 3, false>;
-    return parts ? k_decode_class<0, 4, true> : k_decode_class<0, 3, false>;
+        return parts ? k_decode_class<32, 4, true, NTH> : k_decode_class<32, 3, false, NTH>;
+    return parts ? k_decode_class<0, 4, true, NTH> : k_decode_class<0, 3, false, NTH>;
+}
+
+// split: CTAs per tile (1, 2 or 4)
+decode_fn decode_kernel(int32_t bins, bool parts, int split)
+{
+    if (split == 4)
+        return decode_kernel_nth<NT / 4>(bins, parts);
+    if (split == 2)
+        return decode_kernel_nth<NT / 2>(bins, parts);
+    return decode_kernel_nth<NT>(bins, parts);
+}
+
+// Number of SMs of the current device.
+cudaError_t sm_count(int *sms)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess)
+        err = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    return err;
 }
 
 // The dynamic shared-memory limit is a per-device function attribute: set
@@ -1419,13 +1491,16 @@ cudaError_t ensure_smem_attributes()
         return cudaSuccess;
     const int32_t bins[3] = {16, 32, 0};
     for (int i = 0; i < 3 && err == cudaSuccess; ++i) {
+        // the plan keeps dynamic shared memory below CG_SMEM_LIMIT - 2048,
+        // which leaves room for the kernels' static shared memory
         err = cudaFuncSetAttribute(encode_kernel(bins[i]),
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   CG_SMEM_LIMIT - 1024);
+                                   CG_SMEM_LIMIT - 2048);
         for (int parts = 0; parts < 2 && err == cudaSuccess; ++parts)
-            err = cudaFuncSetAttribute(decode_kernel(bins[i], parts != 0),
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       CG_SMEM_LIMIT - 1024);
+            for (int split = 1; split <= 4 && err == cudaSuccess; split *= 2)
+                err = cudaFuncSetAttribute(decode_kernel(bins[i], parts != 0, split),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           CG_SMEM_LIMIT - 2048);
     }
     if (err == cudaSuccess)
         done.fetch_or(bit);
@@ -1614,9 +1689,20 @@ cudaError_t cg_launch_decode(const cg_plan *p, const cg_encoded *in, uint64_t st
                                          status);
     p->prof.end(stream);
     p->prof.begin(CG_K_DECODE_TILES, stream);
+    int sms = 0;
+    err = sm_count(&sms);
+    if (err != cudaSuccess)
+        return err;
+    // a call with fewer than 1.5 tiles per SM would leave some SMs with two
+    // tiles and others with one (the launch then takes two tiles' time): it
+    // splits each tile's streams over 4 CTAs of 64 threads, which spreads
+    // evenly. With more tiles per SM the imbalance is small and the copies of
+    // the CDF table that a split costs outweigh it.
+    const int split = ((int64_t)ntiles * 2 < (int64_t)sms * 3) ? 4 : 1;
     err = launch_classes(p, stream, [&](const cg_bin_class &cl, cudaStream_t s) {
         const int32_t part_ch = cg_decode_part_channels(p->C, cl.bins);
-        decode_kernel(cl.bins, part_ch < p->C)<<<p->tp.ngroups * cl.count, NT, cl.smem_decode, s>>>(
+        decode_kernel(cl.bins, part_ch < p->C, split)<<<p->tp.ngroups * cl.count * split,
+                                                        NT / split, cl.smem_decode, s>>>(
             p->tp, cl.begin, in->bytestream, stream_bytes, in->lengths, in->cdf, in->amax,
             tile_base, static_cast<uint16_t *>(kv_out), status, part_ch);
     });
