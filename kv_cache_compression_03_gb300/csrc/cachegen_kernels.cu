@@ -431,16 +431,8 @@ __device__ __forceinline__ uint32_t enc_finish(Enc &e)
     return bits;
 }
 
-// Code one token's stream: symbols srow[0..C) with the CDF rows of the
-// shared table. Returns the length in bits; *flag is set when the fast
-// path met a carry it cannot place (then the caller codes it again with
-// EXACT). Reads 16 symbols per load when C is a multiple of 16.
-template <bool EXACT, bool NIB>
-__device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
-                                                const uint16_t *table, int32_t Lp, uint32_t *out,
-                                                uint32_t cap, uint32_t *wp_out, uint32_t *flag)
+__device__ __forceinline__ void enc_init(Enc &e, uint32_t *out, uint32_t cap)
 {
-    Enc e;
     e.x = 0;
     e.d = 0xFFFFFFFFu;
     e.a0 = e.a1 = 0;
@@ -450,11 +442,21 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
     e.hold = 0;
     e.flag = 0;
     e.out = out;
+}
+
+// Code symbols [c_begin, c_begin + C) of a token's symbol row with the CDF
+// rows table[0..C) (row j for symbol c_begin + j). c_begin is a multiple of
+// 32. Reads 16 symbols per load (bytes, C a multiple of 16) or 32 (4-bit
+// codes, C a multiple of 32), else 8.
+template <bool EXACT, bool NIB>
+__device__ __forceinline__ void code_symbols(Enc &e, const uint8_t *srow8, int32_t c_begin,
+                                             int32_t C, const uint16_t *table, int32_t Lp)
+{
     const uint16_t *trow = table;
     if (NIB) {
         // 4-bit codes, 32 per 16-byte load (C is a multiple of 32): byte k
         // of a word holds channels 2k (low half) and 2k + 1 (high half)
-        const uint4 *srow = reinterpret_cast<const uint4 *>(srow8);
+        const uint4 *srow = reinterpret_cast<const uint4 *>(srow8 + c_begin / 2);
         uint4 next = srow[0];
         for (int32_t c0 = 0; c0 < C; c0 += 32) {
             const uint4 v = next;
@@ -473,7 +475,7 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
             }
         }
     } else if ((C & 15) == 0) {
-        const uint4 *srow = reinterpret_cast<const uint4 *>(srow8);
+        const uint4 *srow = reinterpret_cast<const uint4 *>(srow8 + c_begin);
         uint4 next = srow[0];
         for (int32_t c0 = 0; c0 < C; c0 += 16) {
             const uint4 v = next;
@@ -493,7 +495,7 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
             }
         }
     } else {
-        const uint2 *srow = reinterpret_cast<const uint2 *>(srow8);
+        const uint2 *srow = reinterpret_cast<const uint2 *>(srow8 + c_begin);
         uint2 next = srow[0];
         for (int32_t c0 = 0; c0 < C; c0 += 8) {
             const uint2 v = next;
@@ -510,6 +512,20 @@ __device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
             }
         }
     }
+}
+
+// Code one token's stream: symbols srow[0..C) with the CDF rows of the
+// shared table. Returns the length in bits; *flag is set when the fast
+// path met a carry it cannot place (then the caller codes it again with
+// EXACT).
+template <bool EXACT, bool NIB>
+__device__ __forceinline__ uint32_t code_stream(const uint8_t *srow8, int32_t C,
+                                                const uint16_t *table, int32_t Lp, uint32_t *out,
+                                                uint32_t cap, uint32_t *wp_out, uint32_t *flag)
+{
+    Enc e;
+    enc_init(e, out, cap);
+    code_symbols<EXACT, NIB>(e, srow8, 0, C, table, Lp);
     const uint32_t bits = enc_finish<EXACT>(e);
     *wp_out = e.wp;
     *flag = e.flag;
@@ -528,18 +544,47 @@ __device__ __noinline__ uint64_t code_stream_exact(const uint8_t *srow8, int32_t
     return ((uint64_t)wp << 32) | bits;
 }
 
+// Parts path: the fast state `st` raised its flag while coding a part (or
+// while finishing); code that part again exactly from the state `st` held at
+// the part's start. In the fast state the last completed word is held in a
+// register, not stored: store it, then continue in the exact form (which
+// stores every word and pushes carries into stored words).
+template <bool NIB>
+__device__ __noinline__ void code_part_exact(Enc *st, const uint8_t *srow8, int32_t c_begin,
+                                             int32_t C, const uint16_t *table, int32_t Lp,
+                                             bool from_fast)
+{
+    Enc e = *st;
+    if (from_fast && e.wp >= 1 && e.wp - 1 < e.cap)
+        e.out[e.wp - 1] = __byte_perm(e.hold, 0, 0x0123);
+    code_symbols<true, NIB>(e, srow8, c_begin, C, table, Lp);
+    *st = e;
+}
+
+__device__ __noinline__ uint32_t finish_exact(Enc *st)
+{
+    Enc e = *st;
+    const uint32_t bits = enc_finish<true>(e);
+    *st = e;
+    return bits;
+}
+
 // Phase A, counting one block of rows: each thread owns W consecutive
 // channels (W = 4 with 8-byte loads and 4-byte symbol stores; W = 2 and 1
 // for narrower rows).
-template <int NB, int W, bool NIB>
+template <int NB, int W, bool NIB, bool PARTIAL = false>
 __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, int32_t C,
                                             int32_t r0, int32_t nr, const float *fac, float fmax,
-                                            uint16_t *table, int32_t N, uint8_t *sym_tile)
+                                            uint16_t *table, int32_t N, uint8_t *sym_tile,
+                                            int32_t cnt_units = 0)
 {
     const int32_t Lp = N + 1;
     const int32_t units = C / W;
     for (int32_t p = threadIdx.x; p < units; p += NT) {
-        uint16_t *h0 = table + (size_t)(W * p) * Lp;
+        // PARTIAL: only units below cnt_units count (the table holds their
+        // rows); every unit stores its symbols
+        uint16_t *h0 = table + (size_t)(W * (PARTIAL ? min(p, cnt_units - 1) : p)) * Lp;
+        const bool cnt = !PARTIAL || p < cnt_units;
         for (int32_t rb = r0; rb < r0 + nr; rb += kCountBatch) {
             const int32_t nb = min(kCountBatch, r0 + nr - rb);
             if (W == 4 && nb == kCountBatch) {
@@ -558,10 +603,12 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
                     const uint32_t b3 = quantise_bits(__uint_as_float(w[u].y & 0xFFFF0000u), f, fmax);
                     const uint32_t q0 = symbol_of<NB>(b0, N), q1 = symbol_of<NB>(b1, N);
                     const uint32_t q2 = symbol_of<NB>(b2, N), q3 = symbol_of<NB>(b3, N);
-                    h0[q0] += 1;
-                    h0[Lp + q1] += 1;
-                    h0[2 * Lp + q2] += 1;
-                    h0[3 * Lp + q3] += 1;
+                    if (cnt) {
+                        h0[q0] += 1;
+                        h0[Lp + q1] += 1;
+                        h0[2 * Lp + q2] += 1;
+                        h0[3 * Lp + q3] += 1;
+                    }
                     if (NIB) {
                         // four 4-bit codes, channel 4p + i in bits 4i..4i+3
                         // (multiply-adds: q < 16 leaves no carry between codes)
@@ -587,10 +634,12 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
                         const uint32_t q1 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x & 0xFFFF0000u), f, fmax), N);
                         const uint32_t q2 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y << 16), f, fmax), N);
                         const uint32_t q3 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y & 0xFFFF0000u), f, fmax), N);
-                        h0[q0] += 1;
-                        h0[Lp + q1] += 1;
-                        h0[2 * Lp + q2] += 1;
-                        h0[3 * Lp + q3] += 1;
+                        if (cnt) {
+                            h0[q0] += 1;
+                            h0[Lp + q1] += 1;
+                            h0[2 * Lp + q2] += 1;
+                            h0[3 * Lp + q3] += 1;
+                        }
                         if (NIB)
                             reinterpret_cast<uint16_t *>(sym_tile)[p + (size_t)(rb + u) * (C / 4)] =
                                 (uint16_t)(q0 | (q1 << 4) | (q2 << 8) | (q3 << 12));
@@ -612,8 +661,10 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
                         const float f = fac[rb + u];
                         const uint32_t q0 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u] << 16), f, fmax), N);
                         const uint32_t q1 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u] & 0xFFFF0000u), f, fmax), N);
-                        h0[q0] += 1;
-                        h0[Lp + q1] += 1;
+                        if (cnt) {
+                            h0[q0] += 1;
+                            h0[Lp + q1] += 1;
+                        }
                         dst[(size_t)(rb + u) * (C / 2)] = (uint16_t)(q0 | (q1 << 8));
                     }
                 }
@@ -628,7 +679,8 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
                 for (int u = 0; u < kCountBatch; ++u) {
                     if (u < nb) {
                         const uint32_t q = symbol_of<NB>(quantise_bits(__uint_as_float(w[u] << 16), fac[rb + u], fmax), N);
-                        h0[q] += 1;
+                        if (cnt)
+                            h0[q] += 1;
                         dst[(size_t)(rb + u) * C] = (uint8_t)q;
                     }
                 }
@@ -716,9 +768,64 @@ __device__ __forceinline__ void prefetch_rows(const uint16_t *rows, int32_t C, i
         asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 128u * i));
 }
 
+// Phase B for rows [0, nrows) of the table: the integer CDF in place of the
+// histogram. cdf[i] = floor(cum_i * (65536 - N) / n) + i; the floor uses
+// m = ceil(2^32 / n): cum*K < 2^24 and n <= 256 keep the product's error
+// below 2^-8 <= 1/n, under the quotient's distance to the next integer, so
+// (cum*K*m) >> 32 is the exact floor.
+__device__ __forceinline__ void cdf_rows(uint16_t *table, int32_t nrows, int32_t N, int32_t n)
+{
+    const int32_t Lp = N + 1;
+    const uint64_t inv = ((((uint64_t)1) << 32) + (uint64_t)n - 1) / (uint64_t)n;
+    const uint32_t K = 65536u - (uint32_t)N;
+    for (int32_t c = threadIdx.x; c < nrows; c += NT) {
+        uint16_t *row = table + (size_t)c * Lp;
+        uint32_t cum = 0;
+#pragma unroll
+        for (int32_t i = 0; i <= N; ++i) {
+            const uint32_t cnt = (i < N) ? row[i] : 0u;
+            const uint32_t fl = (uint32_t)(((uint64_t)(cum * K) * inv) >> 32);
+            row[i] = (uint16_t)(fl + (uint32_t)i);  // 65536 wraps to 0
+            cum += cnt;
+        }
+    }
+}
+
+// Copy rows [0, nrows) of the table (16-byte multiple) to dst.
+__device__ __forceinline__ void copy_rows_out(uint16_t *dst, const uint16_t *table, int32_t nrows,
+                                              int32_t Lp)
+{
+    const uint32_t nbytes = (uint32_t)nrows * Lp * 2u;
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(table);
+    for (uint32_t i = threadIdx.x; i < nbytes / 16; i += NT)
+        d4[i] = s4[i];
+}
+
+// Inf/NaN values of a reported row quantise to the top symbol N - 1
+// (symbol_of); its upper bound cdf[N] = 65536 is held as 0 in the table.
+// Coding such a tile (its output is undefined) with 65535 as that bound
+// keeps every interval well formed: the top symbol then occurs, so
+// cdf[N - 1] <= 65534 and its width stays >= 1 of 2^16.
+__device__ __forceinline__ void patch_top_bounds(uint16_t *table, int32_t nrows, int32_t N)
+{
+    __syncthreads();
+    for (int32_t c = threadIdx.x; c < nrows; c += NT)
+        table[(size_t)c * (N + 1) + N] = 0xFFFFu;
+    __syncthreads();
+}
+
 // One tile of the encoder. NB > 0 fixes the bin count at compile time
-// (16 and 32 are the presets); NB = 0 reads it from the tile.
-template <int NB>
+// (16 and 32 are the presets); NB = 0 reads it from the tile. PARTS (rows
+// of at least 1024 channels whose CDF table exceeds the shared-memory
+// budget): the table holds part_ch channels at a time (a multiple of 32).
+// Phase A stores every symbol but counts only the first part; each later
+// part is counted from the stored symbols. Each part's CDF rows are built,
+// copied out and used to code that part's channels of every stream, the
+// coder state staying in registers across a block barrier; a stream whose
+// fast path raised its flag in a part codes that part again exactly from
+// the state it held at the part's start, and the rest exactly.
+template <int NB, bool PARTS>
 __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__restrict__ kv,
                                             const cg_tile_params &P, uint8_t *sym_ws,
                                             float *__restrict__ amax_out,
@@ -727,17 +834,19 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
                                             uint8_t *__restrict__ slots,
                                             uint32_t *__restrict__ tile_totals,
                                             uint32_t *__restrict__ status, uint8_t *smem,
-                                            uint32_t *warp_sums, uint32_t *nonfinite)
+                                            uint32_t *warp_sums, uint32_t *nonfinite,
+                                            int32_t part_ch)
 {
     const int32_t C = P.C;
     const int32_t N = NB > 0 ? NB : tl.N;
     const int32_t Lp = N + 1;
     const float fmax = (float)(N / 2 - 1);
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int32_t tab_ch = PARTS ? part_ch : C;
 
-    // shared: table[C][Lp] u16 (histogram, then CDF) | fac[256] f32
+    // shared: table[tab_ch][Lp] u16 (histogram, then CDF) | fac[256] f32
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
-    const uint32_t table_bytes = ((uint32_t)C * Lp * 2u + 15u) & ~15u;
+    const uint32_t table_bytes = ((uint32_t)tab_ch * Lp * 2u + 15u) & ~15u;
     float *fac = reinterpret_cast<float *>(smem + table_bytes);
 
     if (tid == 0)
@@ -781,14 +890,22 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
         uint4 xa[4];
         if (pipelined)
             amax_issue(rows + (size_t)ta * C, C, ta < tl.n, xa);
-        if (nib)
+        if (PARTS) {
+            if (nib)
+                count_block<NB, 4, true, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile,
+                                               part_ch / 4);
+            else
+                count_block<NB, 4, false, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile,
+                                                part_ch / 4);
+        } else if (nib) {
             count_block<NB, 4, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
-        else if (C / 4 >= NT)
+        } else if (C / 4 >= NT) {
             count_block<NB, 4, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
-        else if (C / 2 >= NT)
+        } else if (C / 2 >= NT) {
             count_block<NB, 2, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
-        else
+        } else {
             count_block<NB, 1, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+        }
         const uint32_t ma = pipelined ? amax_finish(xa)
                                       : (ta < tl.n) ? row_absmax(rows + (size_t)ta * C, C) : 0u;
         const int32_t tb = ta + NT / 32;
@@ -799,65 +916,119 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     if (tid == 0 && *nonfinite)
         set_status(status, CG_ERR_NONFINITE);
 
-    // B: CDF in place. cdf[i] = floor(cum_i * (65536 - N) / n) + i; the floor
-    // uses m = ceil(2^32 / n): cum*K < 2^24 and n <= 256 keep the product's
-    // error below 2^-8 <= 1/n, under the quotient's distance to the next
-    // integer, so (cum*K*m) >> 32 is the exact floor.
-    {
-        const uint64_t inv = ((((uint64_t)1) << 32) + (uint64_t)tl.n - 1) / (uint64_t)tl.n;
-        const uint32_t K = 65536u - (uint32_t)N;
-        for (int32_t c = tid; c < C; c += NT) {
-            uint16_t *row = table + (size_t)c * Lp;
-            uint32_t cum = 0;
-#pragma unroll
-            for (int32_t i = 0; i <= N; ++i) {
-                const uint32_t cnt = (i < N) ? row[i] : 0u;
-                const uint32_t fl = (uint32_t)(((uint64_t)(cum * K) * inv) >> 32);
-                row[i] = (uint16_t)(fl + (uint32_t)i);  // 65536 wraps to 0
-                cum += cnt;
+    uint32_t nbytes_stream = 0;
+    const uint32_t cap = (P.slot_stride - 16) / 4;
+    uint32_t *out = reinterpret_cast<uint32_t *>(slots + (tl.first_stream + tid) * (uint64_t)P.slot_stride + 16);
+    const uint8_t *srow = sym_tile + (size_t)tid * row_bytes;
+    if (!PARTS) {
+        // B: CDF in place, copied out as the tile's CDF block ([C][Lp],
+        // 16-byte aligned)
+        cdf_rows(table, C, N, tl.n);
+        __syncthreads();
+        copy_rows_out(cdf_out + tl.cdf_base, table, C, Lp);
+        if (*nonfinite)
+            patch_top_bounds(table, C, N);
+
+        // C: one stream per token
+        if (tid < tl.n) {
+            uint32_t wp = 0, flag = 0;
+            uint32_t bits = nib ? code_stream<false, true>(srow, C, table, Lp, out, cap, &wp, &flag)
+                                : code_stream<false, false>(srow, C, table, Lp, out, cap, &wp, &flag);
+            if (flag) {
+                const uint64_t r = nib ? code_stream_exact<true>(srow, C, table, Lp, out, cap)
+                                       : code_stream_exact<false>(srow, C, table, Lp, out, cap);
+                bits = (uint32_t)r;
+                wp = (uint32_t)(r >> 32);
+            }
+            nbytes_stream = (bits + 7u) / 8u;
+            if (wp > cap)
+                set_status(status, CG_ERR_CAPACITY);
+            lengths[tl.first_stream + tid] = (int32_t)nbytes_stream;
+        }
+    } else {
+        const bool active = tid < tl.n;
+        Enc e;
+        enc_init(e, out, cap);
+        bool exact = false;
+        uint32_t bits = 0;
+        for (int32_t c_begin = 0; c_begin < C; c_begin += part_ch) {
+            const int32_t nch = min(part_ch, C - c_begin);
+            if (c_begin > 0) {
+                // count this part from the stored symbols
+                __syncthreads();  // the previous part's coding is done with the table
+                {
+                    uint4 *t4 = reinterpret_cast<uint4 *>(table);
+                    for (uint32_t i = tid; i < table_bytes / 16; i += NT)
+                        t4[i] = make_uint4(0, 0, 0, 0);
+                }
+                __syncthreads();
+                for (int32_t u = c_begin / 4 + tid; u < (c_begin + nch) / 4; u += NT) {
+                    uint16_t *h0 = table + (size_t)(4 * u - c_begin) * Lp;
+                    for (int32_t r = 0; r < tl.n; ++r) {
+                        const uint8_t *rp = sym_tile + (size_t)r * row_bytes;
+                        uint32_t q0, q1, q2, q3;
+                        if (nib) {
+                            const uint32_t w = reinterpret_cast<const uint16_t *>(rp)[u];
+                            q0 = w & 15u;
+                            q1 = (w >> 4) & 15u;
+                            q2 = (w >> 8) & 15u;
+                            q3 = w >> 12;
+                        } else {
+                            const uint32_t w = reinterpret_cast<const uint32_t *>(rp)[u];
+                            q0 = w & 0xFFu;
+                            q1 = (w >> 8) & 0xFFu;
+                            q2 = (w >> 16) & 0xFFu;
+                            q3 = w >> 24;
+                        }
+                        h0[q0] += 1;
+                        h0[Lp + q1] += 1;
+                        h0[2 * Lp + q2] += 1;
+                        h0[3 * Lp + q3] += 1;
+                    }
+                }
+                __syncthreads();
+            }
+            cdf_rows(table, nch, N, tl.n);
+            __syncthreads();
+            copy_rows_out(cdf_out + tl.cdf_base + (size_t)c_begin * Lp, table, nch, Lp);
+            if (*nonfinite)
+                patch_top_bounds(table, nch, N);
+            if (active) {
+                const bool last = c_begin + nch >= C;
+                if (!exact) {
+                    const Enc save = e;
+                    if (nib)
+                        code_symbols<false, true>(e, srow, c_begin, nch, table, Lp);
+                    else
+                        code_symbols<false, false>(e, srow, c_begin, nch, table, Lp);
+                    if (last)
+                        bits = enc_finish<false>(e);
+                    if (e.flag) {
+                        e = save;
+                        exact = true;
+                        if (nib)
+                            code_part_exact<true>(&e, srow, c_begin, nch, table, Lp, true);
+                        else
+                            code_part_exact<false>(&e, srow, c_begin, nch, table, Lp, true);
+                        if (last)
+                            bits = finish_exact(&e);
+                    }
+                } else {
+                    if (nib)
+                        code_part_exact<true>(&e, srow, c_begin, nch, table, Lp, false);
+                    else
+                        code_part_exact<false>(&e, srow, c_begin, nch, table, Lp, false);
+                    if (last)
+                        bits = finish_exact(&e);
+                }
             }
         }
-    }
-    __syncthreads();
-    {
-        // the tile's CDF block: same [C][Lp] layout, 16-byte aligned
-        const uint32_t nbytes = (uint32_t)C * Lp * 2u;
-        uint4 *dst = reinterpret_cast<uint4 *>(cdf_out + tl.cdf_base);
-        const uint4 *src = reinterpret_cast<const uint4 *>(table);
-        for (uint32_t i = tid; i < nbytes / 16; i += NT)
-            dst[i] = src[i];
-    }
-    if (*nonfinite) {
-        // inf/NaN values of a reported row quantise to the top symbol N - 1
-        // (symbol_of); its upper bound cdf[N] = 65536 is held as 0 in the
-        // table. Coding such a tile (its output is undefined) with 65535 as
-        // that bound keeps every interval well formed: the top symbol then
-        // occurs, so cdf[N - 1] <= 65534 and its width stays >= 1 of 2^16.
-        __syncthreads();
-        for (int32_t c = tid; c < C; c += NT)
-            table[(size_t)c * Lp + N] = 0xFFFFu;
-        __syncthreads();
-    }
-
-    // C: one stream per token
-    uint32_t nbytes_stream = 0;
-    if (tid < tl.n) {
-        const uint8_t *srow = sym_tile + (size_t)tid * row_bytes;
-        uint32_t *out = reinterpret_cast<uint32_t *>(slots + (tl.first_stream + tid) * (uint64_t)P.slot_stride + 16);
-        const uint32_t cap = (P.slot_stride - 16) / 4;
-        uint32_t wp = 0, flag = 0;
-        uint32_t bits = nib ? code_stream<false, true>(srow, C, table, Lp, out, cap, &wp, &flag)
-                            : code_stream<false, false>(srow, C, table, Lp, out, cap, &wp, &flag);
-        if (flag) {
-            const uint64_t r = nib ? code_stream_exact<true>(srow, C, table, Lp, out, cap)
-                                   : code_stream_exact<false>(srow, C, table, Lp, out, cap);
-            bits = (uint32_t)r;
-            wp = (uint32_t)(r >> 32);
+        if (active) {
+            nbytes_stream = (bits + 7u) / 8u;
+            if (e.wp > cap)
+                set_status(status, CG_ERR_CAPACITY);
+            lengths[tl.first_stream + tid] = (int32_t)nbytes_stream;
         }
-        nbytes_stream = (bits + 7u) / 8u;
-        if (wp > cap)
-            set_status(status, CG_ERR_CAPACITY);
-        lengths[tl.first_stream + tid] = (int32_t)nbytes_stream;
     }
     uint32_t total = 0;
     block_exclusive_scan(nbytes_stream, warp_sums, &total);
@@ -866,20 +1037,21 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
 }
 
 // Encoder tiles of one launch class (NB bins; 0 = any), at least MINB
-// CTAs per SM.
-template <int NB, int MINB>
+// CTAs per SM; PARTS as in encode_tile.
+template <int NB, int MINB, bool PARTS>
 __global__ void __launch_bounds__(NT, MINB)
     k_encode_class(const uint16_t *__restrict__ kv, const cg_tile_params P, int32_t cls_begin,
                    uint8_t *sym_ws, float *__restrict__ amax_out, uint16_t *__restrict__ cdf_out,
                    int32_t *__restrict__ lengths, uint8_t *__restrict__ slots,
-                   uint32_t *__restrict__ tile_totals, uint32_t *__restrict__ status)
+                   uint32_t *__restrict__ tile_totals, uint32_t *__restrict__ status,
+                   int32_t part_ch)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t warp_sums[NT / 32];
     __shared__ uint32_t nonfinite;
     const Tile tl = tile_of_class(P, cls_begin, blockIdx.x);
-    encode_tile<NB>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals, status,
-                    smem, warp_sums, &nonfinite);
+    encode_tile<NB, PARTS>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals,
+                           status, smem, warp_sums, &nonfinite, part_ch);
 }
 
 // Exclusive scan of the per-tile byte totals (one CTA), plus the grand
@@ -1432,18 +1604,18 @@ __global__ void __launch_bounds__(NTH, MINB *(NT / NTH))
 // The kernel of each class, by bin count: 16 and 32 have specialised
 // bodies and their own register budgets.
 typedef void (*encode_fn)(const uint16_t *, const cg_tile_params, int32_t, uint8_t *, float *,
-                          uint16_t *, int32_t *, uint8_t *, uint32_t *, uint32_t *);
+                          uint16_t *, int32_t *, uint8_t *, uint32_t *, uint32_t *, int32_t);
 typedef void (*decode_fn)(const cg_tile_params, int32_t, const uint8_t *, uint64_t,
                           const int32_t *, const uint16_t *, const float *, const uint64_t *,
                           uint16_t *, uint32_t *, int32_t);
 
-encode_fn encode_kernel(int32_t bins)
+encode_fn encode_kernel(int32_t bins, bool parts)
 {
     if (bins == 16)
-        return k_encode_class<16, 4>;
+        return parts ? k_encode_class<16, 4, true> : k_encode_class<16, 4, false>;
     if (bins == 32)
-        return k_encode_class<32, 3>;
-    return k_encode_class<0, 3>;
+        return parts ? k_encode_class<32, 4, true> : k_encode_class<32, 3, false>;
+    return parts ? k_encode_class<0, 4, true> : k_encode_class<0, 3, false>;
 }
 
 template <int NTH>
@@ -1493,9 +1665,10 @@ cudaError_t ensure_smem_attributes()
     for (int i = 0; i < 3 && err == cudaSuccess; ++i) {
         // the plan keeps dynamic shared memory below CG_SMEM_LIMIT - 2048,
         // which leaves room for the kernels' static shared memory
-        err = cudaFuncSetAttribute(encode_kernel(bins[i]),
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   CG_SMEM_LIMIT - 2048);
+        for (int parts = 0; parts < 2 && err == cudaSuccess; ++parts)
+            err = cudaFuncSetAttribute(encode_kernel(bins[i], parts != 0),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       CG_SMEM_LIMIT - 2048);
         for (int parts = 0; parts < 2 && err == cudaSuccess; ++parts)
             for (int split = 1; split <= 4 && err == cudaSuccess; split *= 2)
                 err = cudaFuncSetAttribute(decode_kernel(bins[i], parts != 0, split),
@@ -1509,9 +1682,19 @@ cudaError_t ensure_smem_attributes()
 
 }  // namespace
 
+int32_t cg_encode_part_channels(int32_t C, int32_t bins)
+{
+    const size_t table = (size_t)C * (bins + 1) * 2;
+    if (C < 4 * CG_TILE_THREADS || C % 32 != 0 || table <= CG_DECODE_TABLE_BUDGET)
+        return C;
+    const int32_t parts = (int32_t)((table + CG_DECODE_TABLE_BUDGET - 1) / CG_DECODE_TABLE_BUDGET);
+    return ((C + parts - 1) / parts + 31) / 32 * 32;
+}
+
 size_t cg_smem_encode(int32_t C, int32_t bins)
 {
-    return (((size_t)C * (bins + 1) * 2 + 15) & ~(size_t)15) + CG_GROUP_TOKENS * sizeof(float);
+    const size_t ch = (size_t)cg_encode_part_channels(C, bins);
+    return ((ch * (bins + 1) * 2 + 15) & ~(size_t)15) + CG_GROUP_TOKENS * sizeof(float);
 }
 
 int32_t cg_decode_part_channels(int32_t C, int32_t bins)
@@ -1648,9 +1831,10 @@ cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const c
         return err;
     p->prof.begin(CG_K_ENCODE_TILES, stream);
     err = launch_classes(p, stream, [&](const cg_bin_class &cl, cudaStream_t s) {
-        encode_kernel(cl.bins)<<<p->tp.ngroups * cl.count, NT, cl.smem_encode, s>>>(
+        const int32_t part_ch = cg_encode_part_channels(p->C, cl.bins);
+        encode_kernel(cl.bins, part_ch < p->C)<<<p->tp.ngroups * cl.count, NT, cl.smem_encode, s>>>(
             static_cast<const uint16_t *>(kv), p->tp, cl.begin, sym, out->amax, out->cdf,
-            out->lengths, slots, tile_totals, status);
+            out->lengths, slots, tile_totals, status, part_ch);
     });
     p->prof.end(stream);
     if (err != cudaSuccess)

@@ -118,3 +118,6 @@ size_t cg_smem_decode(int32_t C, int32_t bins);
 // that several CTAs fit on an SM; channels per part (C when one part).
 #define CG_DECODE_TABLE_BUDGET (36 * 1024)
 int32_t cg_decode_part_channels(int32_t C, int32_t bins);
+// The encoder's channels per part (rows of at least 1024 channels, a
+// multiple of 32; C when one part).
+int32_t cg_encode_part_channels(int32_t C, int32_t bins);

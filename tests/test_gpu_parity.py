@@ -117,6 +117,11 @@ EDGE = [
     (2, 256, 8, 128, 256, [(0, 2, 16)], [(0, 2, 16)], "bimodal"),   # 4-bit codes, carry runs
     (1, 300, 8, 160, 256, [(0, 1, 16)], [(0, 1, 16)], "extreme"),   # C = 1280, ragged group
     (1, 100, 3, 344, 256, [(0, 1, 16)], [(0, 1, 16)], "normal"),    # C = 1032: byte codes
+    # CDF tables above the shared-memory budget, coded and decoded in channel
+    # parts: 64 bins (4 parts), 48 bins (3 parts, the last one shorter)
+    (1, 300, 8, 128, 256, [(0, 1, 64)], [(0, 1, 48)], "normal"),
+    (1, 300, 8, 128, 256, [(0, 1, 64)], [(0, 1, 32)], "sparse"),    # parts + exact re-codes
+    (1, 260, 8, 128, 256, [(0, 1, 64)], [(0, 1, 32)], "bimodal"),   # parts + carry runs
 ]
 
 
