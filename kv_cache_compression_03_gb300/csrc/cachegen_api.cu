@@ -259,7 +259,9 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
         // 16-bin symbols (at most 14) as 4-bit codes when the encoder's
         // four-channels-per-thread path runs and rows stay 16-byte aligned
         tp.nib_begin = tp.nib_end = 0;
-        if (C >= 4 * CG_TILE_THREADS && C % 32 == 0)
+        int32_t w16 = 0, r16 = 0;
+        cg_count_layout(C, 16, &w16, &r16);
+        if (w16 == 4 && C % 32 == 0)
             for (const cg_bin_class &cl : p->classes)
                 if (cl.bins == 16) {
                     tp.nib_begin = cl.begin;

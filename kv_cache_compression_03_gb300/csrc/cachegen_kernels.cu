@@ -689,6 +689,73 @@ __device__ __forceinline__ void count_block(const uint16_t *__restrict__ rows, i
     }
 }
 
+// Phase A, counting one block of rows for rows under 4 * NT channels
+// (cg_count_layout): R groups of U = C / W threads; group g counts rows
+// r0 + g, r0 + g + R, ... of the block into its own copy of the histogram
+// (copy g at table + g * C * Lp) and stores their symbols.
+template <int NB, int W, bool NIB, int R>
+__device__ __forceinline__ void count_block_groups(const uint16_t *__restrict__ rows, int32_t C,
+                                                   int32_t r0, int32_t nr, const float *fac,
+                                                   float fmax, uint16_t *table, int32_t N,
+                                                   uint8_t *sym_tile)
+{
+    const int32_t Lp = N + 1;
+    const int32_t U = C / W;
+    const int32_t g = threadIdx.x / U, p = threadIdx.x - g * U;
+    uint16_t *h0 = table + (size_t)g * C * Lp + (size_t)(W * p) * Lp;
+    constexpr int kRows = kRowsPerBlock / R;
+    if (W == 4) {
+        const uint2 *src = reinterpret_cast<const uint2 *>(rows) + p;
+        uint2 w[kRows];
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+            const int32_t r = r0 + g + R * u;
+            w[u] = (r < r0 + nr) ? __ldg(src + (size_t)r * (C / 4)) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+            const int32_t r = r0 + g + R * u;
+            if (r < r0 + nr) {
+                const float f = fac[r];
+                const uint32_t q0 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x << 16), f, fmax), N);
+                const uint32_t q1 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x & 0xFFFF0000u), f, fmax), N);
+                const uint32_t q2 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y << 16), f, fmax), N);
+                const uint32_t q3 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y & 0xFFFF0000u), f, fmax), N);
+                h0[q0] += 1;
+                h0[Lp + q1] += 1;
+                h0[2 * Lp + q2] += 1;
+                h0[3 * Lp + q3] += 1;
+                if (NIB)
+                    reinterpret_cast<uint16_t *>(sym_tile)[p + (size_t)r * (C / 4)] =
+                        (uint16_t)(q0 + 16u * q1 + 256u * q2 + 4096u * q3);
+                else
+                    reinterpret_cast<uint32_t *>(sym_tile)[p + (size_t)r * (C / 4)] =
+                        __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
+            }
+        }
+    } else {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(rows) + p;
+        uint32_t w[kRows];
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+            const int32_t r = r0 + g + R * u;
+            w[u] = (r < r0 + nr) ? __ldg(src + (size_t)r * (C / 2)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+            const int32_t r = r0 + g + R * u;
+            if (r < r0 + nr) {
+                const float f = fac[r];
+                const uint32_t q0 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u] << 16), f, fmax), N);
+                const uint32_t q1 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u] & 0xFFFF0000u), f, fmax), N);
+                h0[q0] += 1;
+                h0[Lp + q1] += 1;
+                reinterpret_cast<uint16_t *>(sym_tile)[p + (size_t)r * (C / 2)] = (uint16_t)(q0 | (q1 << 8));
+            }
+        }
+    }
+}
+
 // Phase A, largest |x| of one row (one warp) as bf16 bits, in every lane:
 // the lanes' maxima over the bf16 bit patterns with the sign cleared
 // (finite values order like their patterns), then one warp reduction.
@@ -773,17 +840,26 @@ __device__ __forceinline__ void prefetch_rows(const uint16_t *rows, int32_t C, i
 // m = ceil(2^32 / n): cum*K < 2^24 and n <= 256 keep the product's error
 // below 2^-8 <= 1/n, under the quotient's distance to the next integer, so
 // (cum*K*m) >> 32 is the exact floor.
-__device__ __forceinline__ void cdf_rows(uint16_t *table, int32_t nrows, int32_t N, int32_t n)
+// With R > 1 the counts are the sum of R histogram copies, nrows * Lp
+// entries apart (the CDF goes to copy 0).
+__device__ __forceinline__ void cdf_rows(uint16_t *table, int32_t nrows, int32_t N, int32_t n,
+                                         int32_t R = 1)
 {
     const int32_t Lp = N + 1;
     const uint64_t inv = ((((uint64_t)1) << 32) + (uint64_t)n - 1) / (uint64_t)n;
     const uint32_t K = 65536u - (uint32_t)N;
+    const size_t copy = (size_t)nrows * Lp;
     for (int32_t c = threadIdx.x; c < nrows; c += NT) {
         uint16_t *row = table + (size_t)c * Lp;
         uint32_t cum = 0;
 #pragma unroll
         for (int32_t i = 0; i <= N; ++i) {
-            const uint32_t cnt = (i < N) ? row[i] : 0u;
+            uint32_t cnt = 0;
+            if (i < N) {
+                cnt = row[i];
+                for (int32_t g = 1; g < R; ++g)
+                    cnt += row[i + g * copy];
+            }
             const uint32_t fl = (uint32_t)(((uint64_t)(cum * K) * inv) >> 32);
             row[i] = (uint16_t)(fl + (uint32_t)i);  // 65536 wraps to 0
             cum += cnt;
@@ -843,10 +919,14 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     const float fmax = (float)(N / 2 - 1);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int32_t tab_ch = PARTS ? part_ch : C;
+    int32_t cw = 4, cr = 1;  // counting layout (cg_count_layout)
+    if (!PARTS)
+        cg_count_layout(C, N, &cw, &cr);
 
-    // shared: table[tab_ch][Lp] u16 (histogram, then CDF) | fac[256] f32
+    // shared: cr x table[tab_ch][Lp] u16 (histogram copies; then the CDF in
+    // copy 0) | fac[256] f32
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
-    const uint32_t table_bytes = ((uint32_t)tab_ch * Lp * 2u + 15u) & ~15u;
+    const uint32_t table_bytes = ((uint32_t)cr * tab_ch * Lp * 2u + 15u) & ~15u;
     float *fac = reinterpret_cast<float *>(smem + table_bytes);
 
     if (tid == 0)
@@ -897,14 +977,39 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
             else
                 count_block<NB, 4, false, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile,
                                                 part_ch / 4);
-        } else if (nib) {
-            count_block<NB, 4, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
-        } else if (C / 4 >= NT) {
-            count_block<NB, 4, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
-        } else if (C / 2 >= NT) {
-            count_block<NB, 2, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+        } else if (cr == 1) {
+            if (nib)
+                count_block<NB, 4, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            else if (cw == 4)
+                count_block<NB, 4, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            else if (cw == 2)
+                count_block<NB, 2, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            else
+                count_block<NB, 1, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+        } else if (cw == 4) {
+            if (cr == 2) {
+                if (nib)
+                    count_block_groups<NB, 4, true, 2>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                else
+                    count_block_groups<NB, 4, false, 2>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            } else if (cr == 4) {
+                if (nib)
+                    count_block_groups<NB, 4, true, 4>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                else
+                    count_block_groups<NB, 4, false, 4>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            } else {
+                if (nib)
+                    count_block_groups<NB, 4, true, 8>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                else
+                    count_block_groups<NB, 4, false, 8>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            }
         } else {
-            count_block<NB, 1, false>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            if (cr == 2)
+                count_block_groups<NB, 2, false, 2>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            else if (cr == 4)
+                count_block_groups<NB, 2, false, 4>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            else
+                count_block_groups<NB, 2, false, 8>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
         }
         const uint32_t ma = pipelined ? amax_finish(xa)
                                       : (ta < tl.n) ? row_absmax(rows + (size_t)ta * C, C) : 0u;
@@ -923,7 +1028,7 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     if (!PARTS) {
         // B: CDF in place, copied out as the tile's CDF block ([C][Lp],
         // 16-byte aligned)
-        cdf_rows(table, C, N, tl.n);
+        cdf_rows(table, C, N, tl.n, cr);
         __syncthreads();
         copy_rows_out(cdf_out + tl.cdf_base, table, C, Lp);
         if (*nonfinite)
@@ -1703,7 +1808,10 @@ int32_t cg_encode_part_channels(int32_t C, int32_t bins)
 size_t cg_smem_encode(int32_t C, int32_t bins)
 {
     const size_t ch = (size_t)cg_encode_part_channels(C, bins);
-    return ((ch * (bins + 1) * 2 + 15) & ~(size_t)15) + CG_GROUP_TOKENS * sizeof(float);
+    int32_t w = 0, r = 1;
+    if (ch == (size_t)C)
+        cg_count_layout(C, bins, &w, &r);
+    return (((size_t)r * ch * (bins + 1) * 2 + 15) & ~(size_t)15) + CG_GROUP_TOKENS * sizeof(float);
 }
 
 int32_t cg_decode_part_channels(int32_t C, int32_t bins)

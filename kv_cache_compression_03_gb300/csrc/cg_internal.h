@@ -121,3 +121,28 @@ int32_t cg_decode_part_channels(int32_t C, int32_t bins);
 // The encoder's channels per part (rows of at least 1024 channels, a
 // multiple of 32; C when one part).
 int32_t cg_encode_part_channels(int32_t C, int32_t bins);
+
+// Counting layout of the encoder's phase A for rows of C channels at `bins`
+// bins: each counting thread owns W consecutive channels; for rows under
+// 4 * CG_TILE_THREADS channels, R groups of C / W threads (R * C / W =
+// CG_TILE_THREADS, R <= 8) count different rows into private copies of the
+// histogram, which phase B adds up (R copies must fit the table budget).
+__host__ __device__ inline void cg_count_layout(int32_t C, int32_t bins, int32_t *W, int32_t *R)
+{
+    *R = 1;
+    if (C >= 4 * CG_TILE_THREADS) {
+        *W = 4;
+        return;
+    }
+    const int64_t table = (int64_t)C * (bins + 1) * 2;
+    for (int32_t w = 4; w >= 2; w >>= 1) {
+        const int32_t u = C / w;
+        if (C % w == 0 && u <= CG_TILE_THREADS && CG_TILE_THREADS % u == 0 &&
+            CG_TILE_THREADS / u <= 8 && (CG_TILE_THREADS / u) * table <= CG_DECODE_TABLE_BUDGET) {
+            *W = w;
+            *R = CG_TILE_THREADS / u;
+            return;
+        }
+    }
+    *W = (C >= 2 * CG_TILE_THREADS) ? 2 : 1;
+}
