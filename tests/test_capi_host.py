@@ -105,7 +105,6 @@ def test_plan_rejects_bad_specs(orc, k, v):
     ((32, 1024, 1, 12, 256), cg.CG_ERR_INVALID_ARG),     # C not a multiple of 8
     ((32, 1024, 64, 128, 256), cg.CG_ERR_UNSUPPORTED),   # C = 8192 > 4096
     ((300, 16, 8, 128, 256), cg.CG_ERR_UNSUPPORTED),     # more than 256 layers
-    ((2, 16, 32, 128, 256), cg.CG_ERR_UNSUPPORTED),      # C = 4096 at 32 bins: CDF table too big
 ])
 def test_plan_rejects_bad_shapes(args, code):
     L = args[0]
@@ -113,6 +112,17 @@ def test_plan_rejects_bad_shapes(args, code):
     with pytest.raises(cg.CacheGenError) as e:
         cg.cg_plan_create(*args, k, v)
     assert e.value.status == code
+
+
+def test_large_tables_are_planned_in_channel_parts():
+    """CDF tables beyond shared memory (C = 4096 at 32 and 64 bins) are coded
+    and decoded in channel parts, so every shape up to 4096 channels plans."""
+    for bins in (16, 32, 64):
+        plan = cg.cg_plan_create(2, 16, 32, 128, 256, [(0, 2, bins)], [(0, 2, bins)])
+        try:
+            assert cg.cg_plan_sizes(plan).workspace_bytes > 0
+        finally:
+            cg.cg_plan_destroy(plan)
 
 
 def test_preset_specs():

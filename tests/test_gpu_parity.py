@@ -122,6 +122,11 @@ EDGE = [
     (1, 300, 8, 128, 256, [(0, 1, 64)], [(0, 1, 48)], "normal"),
     (1, 300, 8, 128, 256, [(0, 1, 64)], [(0, 1, 32)], "sparse"),    # parts + exact re-codes
     (1, 260, 8, 128, 256, [(0, 1, 64)], [(0, 1, 32)], "bimodal"),   # parts + carry runs
+    (1, 64, 32, 128, 64, [(0, 1, 32)], [(0, 1, 64)], "normal"),     # C = 4096: 8 and 15 parts
+    # rows under 1024 channels counted by row groups into private histograms
+    (2, 300, 1, 128, 256, [(0, 2, 16)], [(0, 2, 32)], "normal"),    # C = 128: 8 / 4 groups
+    (2, 300, 1, 64, 256, [(0, 2, 16)], [(0, 2, 8)], "sparse"),      # C = 64: 8 groups of 32
+    (1, 300, 4, 128, 256, [(0, 1, 16)], [(0, 1, 32)], "extreme"),   # C = 512: 2 groups
 ]
 
 
