@@ -901,7 +901,7 @@ __device__ __forceinline__ void patch_top_bounds(uint16_t *table, int32_t nrows,
 // coder state staying in registers across a block barrier; a stream whose
 // fast path raised its flag in a part codes that part again exactly from
 // the state it held at the part's start, and the rest exactly.
-template <int NB, bool PARTS>
+template <int NB, bool PARTS, bool GROUPS>
 __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__restrict__ kv,
                                             const cg_tile_params &P, uint8_t *sym_ws,
                                             float *__restrict__ amax_out,
@@ -919,9 +919,11 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
     const float fmax = (float)(N / 2 - 1);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int32_t tab_ch = PARTS ? part_ch : C;
-    int32_t cw = 4, cr = 1;  // counting layout (cg_count_layout)
+    int32_t cw = 4, cr = 1;  // counting layout (cg_count_layout; GROUPS: cr > 1)
     if (!PARTS)
         cg_count_layout(C, N, &cw, &cr);
+    if (!GROUPS)
+        cr = 1;
 
     // shared: cr x table[tab_ch][Lp] u16 (histogram copies; then the CDF in
     // copy 0) | fac[256] f32
@@ -977,7 +979,7 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
             else
                 count_block<NB, 4, false, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile,
                                                 part_ch / 4);
-        } else if (cr == 1) {
+        } else if (!GROUPS || cr == 1) {
             if (nib)
                 count_block<NB, 4, true>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
             else if (cw == 4)
@@ -1142,8 +1144,9 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
 }
 
 // Encoder tiles of one launch class (NB bins; 0 = any), at least MINB
-// CTAs per SM; PARTS as in encode_tile.
-template <int NB, int MINB, bool PARTS>
+// CTAs per SM; PARTS as in encode_tile; GROUPS: rows counted by row groups
+// (cg_count_layout gives R > 1).
+template <int NB, int MINB, bool PARTS, bool GROUPS>
 __global__ void __launch_bounds__(NT, MINB)
     k_encode_class(const uint16_t *__restrict__ kv, const cg_tile_params P, int32_t cls_begin,
                    uint8_t *sym_ws, float *__restrict__ amax_out, uint16_t *__restrict__ cdf_out,
@@ -1155,8 +1158,8 @@ __global__ void __launch_bounds__(NT, MINB)
     __shared__ uint32_t warp_sums[NT / 32];
     __shared__ uint32_t nonfinite;
     const Tile tl = tile_of_class(P, cls_begin, blockIdx.x);
-    encode_tile<NB, PARTS>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots, tile_totals,
-                           status, smem, warp_sums, &nonfinite, part_ch);
+    encode_tile<NB, PARTS, GROUPS>(tl, kv, P, sym_ws, amax_out, cdf_out, lengths, slots,
+                                   tile_totals, status, smem, warp_sums, &nonfinite, part_ch);
 }
 
 // Exclusive scan of the per-tile byte totals (one CTA), plus the grand
@@ -1723,13 +1726,27 @@ typedef void (*decode_fn)(const cg_tile_params, int32_t, const uint8_t *, uint64
                           const int32_t *, const uint16_t *, const float *, const uint64_t *,
                           uint16_t *, uint32_t *, int32_t);
 
-encode_fn encode_kernel(int32_t bins, bool parts)
+encode_fn encode_kernel(int32_t bins, bool parts, bool groups)
 {
     if (bins == 16)
-        return parts ? k_encode_class<16, 4, true> : k_encode_class<16, 4, false>;
+        return parts    ? k_encode_class<16, 4, true, false>
+               : groups ? k_encode_class<16, 4, false, true>
+                        : k_encode_class<16, 4, false, false>;
     if (bins == 32)
-        return parts ? k_encode_class<32, 4, true> : k_encode_class<32, 3, false>;
-    return parts ? k_encode_class<0, 4, true> : k_encode_class<0, 3, false>;
+        return parts    ? k_encode_class<32, 4, true, false>
+               : groups ? k_encode_class<32, 3, false, true>
+                        : k_encode_class<32, 3, false, false>;
+    return parts    ? k_encode_class<0, 4, true, false>
+           : groups ? k_encode_class<0, 3, false, true>
+                    : k_encode_class<0, 3, false, false>;
+}
+
+// whether a class of `bins` bins counts by row groups at C channels
+bool encode_groups(int32_t C, int32_t bins)
+{
+    int32_t w = 0, r = 1;
+    cg_count_layout(C, bins, &w, &r);
+    return r > 1;
 }
 
 template <int NTH>
@@ -1779,8 +1796,8 @@ cudaError_t ensure_smem_attributes()
     for (int i = 0; i < 3 && err == cudaSuccess; ++i) {
         // the plan keeps dynamic shared memory below CG_SMEM_LIMIT - 2048,
         // which leaves room for the kernels' static shared memory
-        for (int parts = 0; parts < 2 && err == cudaSuccess; ++parts)
-            err = cudaFuncSetAttribute(encode_kernel(bins[i], parts != 0),
+        for (int v = 0; v < 3 && err == cudaSuccess; ++v)
+            err = cudaFuncSetAttribute(encode_kernel(bins[i], v == 1, v == 2),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        CG_SMEM_LIMIT - 2048);
         for (int parts = 0; parts < 2 && err == cudaSuccess; ++parts)
@@ -1949,7 +1966,8 @@ cudaError_t cg_launch_encode(const cg_plan *p, const void *kv, void *ws, const c
     p->prof.begin(CG_K_ENCODE_TILES, stream);
     err = launch_classes(p, stream, [&](const cg_bin_class &cl, cudaStream_t s) {
         const int32_t part_ch = cg_encode_part_channels(p->C, cl.bins);
-        encode_kernel(cl.bins, part_ch < p->C)<<<p->tp.ngroups * cl.count, NT, cl.smem_encode, s>>>(
+        encode_kernel(cl.bins, part_ch < p->C, encode_groups(p->C, cl.bins))<<<
+            p->tp.ngroups * cl.count, NT, cl.smem_encode, s>>>(
             static_cast<const uint16_t *>(kv), p->tp, cl.begin, sym, out->amax, out->cdf,
             out->lengths, slots, tile_totals, status, part_ch);
     });
