@@ -951,6 +951,50 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
                         (uint64_t)tl.t0 * row_bytes;
     const int32_t nblocks = (tl.n + kRowsPerBlock - 1) / kRowsPerBlock;
 
+    if (GROUPS && C <= 512) {
+        // A for rows of at most 512 channels counted by row groups (a tile of
+        // at most 256 KB, which stays in L2 between the passes): the maxima
+        // and factors of all rows first (a warp per two rows at a time), then
+        // every row counted, with no block barriers in between (each thread
+        // owns its histogram rows)
+        for (int32_t ra = 2 * warp; ra < tl.n; ra += NT / 16) {
+            const int32_t rb = ra + 1;
+            const uint32_t ma = row_absmax(rows + (size_t)ra * C, C);
+            const uint32_t mb = (rb < tl.n) ? row_absmax(rows + (size_t)rb * C, C) : 0u;
+            store_factors(ra, ma, rb, mb, tl.n, fmax, fac, amax_row, nonfinite);
+        }
+        __syncthreads();
+        for (int32_t b = 0; b < nblocks; ++b) {
+            const int32_t r0 = b * kRowsPerBlock;
+            const int32_t nr = min(kRowsPerBlock, tl.n - r0);
+            if (cw == 4) {
+                if (cr == 2) {
+                    if (nib)
+                        count_block_groups<NB, 4, true, 2>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                    else
+                        count_block_groups<NB, 4, false, 2>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                } else if (cr == 4) {
+                    if (nib)
+                        count_block_groups<NB, 4, true, 4>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                    else
+                        count_block_groups<NB, 4, false, 4>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                } else {
+                    if (nib)
+                        count_block_groups<NB, 4, true, 8>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                    else
+                        count_block_groups<NB, 4, false, 8>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                }
+            } else {
+                if (cr == 2)
+                    count_block_groups<NB, 2, false, 2>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                else if (cr == 4)
+                    count_block_groups<NB, 2, false, 4>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+                else
+                    count_block_groups<NB, 2, false, 8>(rows, C, r0, nr, fac, fmax, table, N, sym_tile);
+            }
+        }
+        __syncthreads();
+    } else {
     // A: amax of block 0; then per step, count block b while the loads for
     // block b + 1's amax are in flight (one row per warp), and ask L2 for
     // block b + 2
@@ -1019,6 +1063,7 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
         const uint32_t mb = (tb < tl.n) ? row_absmax(rows + (size_t)tb * C, C) : 0u;
         store_factors(ta, ma, tb, mb, tl.n, fmax, fac, amax_row, nonfinite);
         __syncthreads();
+    }
     }
     if (tid == 0 && *nonfinite)
         set_status(status, CG_ERR_NONFINITE);
