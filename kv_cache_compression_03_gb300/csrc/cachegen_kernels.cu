@@ -13,25 +13,35 @@
 // concurrently on the caller's stream and a forked side stream. Encode
 // (then a tile scan and a pack):
 //   A  blocks of 16 token rows: warp per row computes amax over the C
-//      channels (16-byte loads; |x| maximum on bf16 bit patterns) and the
-//      row's scale factor; then a thread per four channels re-reads the
-//      block (L1/L2-resident), quantises, counts into its own shared-memory
-//      histogram rows (no atomics) and writes the symbols to a scratch row
-//      per stream. The next block's amax overlaps this block's counting.
+//      channels (16-byte loads; |x| maximum on bf16 bit patterns, one warp
+//      reduction) and the row's scale factor; then a thread per four
+//      channels re-reads the block (L1/L2-resident), quantises (the
+//      rounding to an integer as an fp32 addition of 1.5 * 2^23), counts
+//      into its own shared-memory histogram rows (no atomics) and writes
+//      the symbols to a scratch row per stream (4-bit codes for 16 bins,
+//      else bytes). The next block's amax overlaps this block's counting.
+//      Rows under 1024 channels are counted by row groups, each group into
+//      its own histogram copy (cg_count_layout); at <= 512 channels the
+//      maxima of all rows come first and the counting runs without block
+//      barriers.
 //   B  thread per channel: integer CDF in place of the histogram, copied
 //      out as the tile's CDF block.
 //   C  thread per token: arithmetic-code the token's stream over the C
 //      channels with the shared-memory CDF rows (see Enc); completed words
 //      are taken out of the bit buffer once per kStoreEvery symbols.
-// Pack: block scan of the tile's lengths + the tile's base, then the
-// slots are copied to their packed position. Decode: per tile, the CDF
-// block is staged in shared memory, the lengths are scanned, and each
-// thread decodes one stream (binary search with the coder's exact
-// comparison; the bit buffer refilled once per kRefillEvery symbols) and
-// writes the dequantised bf16 row. A stream whose batch of symbols over- or
-// under-runs the 64-bit bit buffer (possible only for runs of a group's
-// rarest symbols) is redone on an exact path that checks after every
-// symbol.
+//   Tables larger than the shared-memory budget (32 and 64 bins at 1024
+//   channels) go through phases B and C in channel parts, the coder state
+//   carried in registers across a block barrier.
+// Pack: block scan of the tile's lengths + the tile's base, then each warp
+// copies four streams at a time from their slots to their packed position.
+// Decode: per tile, the CDF block (or one channel part at a time) is
+// staged in shared memory, the lengths are scanned, and each thread decodes
+// one stream (binary search with the coder's exact comparison; the bit
+// buffer refilled once per kRefillEvery symbols) and writes the
+// dequantised bf16 row; calls with few tiles split each tile's streams over
+// four CTAs. A stream (or part) whose batch of symbols over- or under-runs
+// the 64-bit bit buffer (possible only for runs of a group's rarest
+// symbols) is redone on an exact path that checks after every symbol.
 //
 // No kernel waits on another block, and every loop is bounded by the
 // tile's token and channel counts or the alphabet size.
