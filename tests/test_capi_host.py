@@ -373,3 +373,49 @@ def test_status_buffers_are_checked_before_the_call():
         cg.cg_int8_encode(small, 1, 8, small, small, small)
     with pytest.raises(ValueError):
         cg.cg_int8_encode(small, 1, 8, small, small, None)
+
+
+def _count_layout(C, bins):
+    """The encoder's counting layout rule, restated: (channels per thread,
+    row groups)."""
+    if C >= 1024:
+        return 4, 1
+    table = C * (bins + 1) * 2
+    for w in (4, 2):
+        u = C // w
+        if C % w == 0 and u <= 256 and 256 % u == 0 and 256 // u <= 8 and \
+                (256 // u) * table <= 36 * 1024:
+            return w, 256 // u
+    return (2 if C >= 512 else 1), 1
+
+
+@pytest.mark.parametrize("L,T,H,D,k,v", [
+    (32, 1024, 8, 128, None, None),                      # 16-bin pairs as 4-bit codes
+    (40, 700, 2, 128, [(0, 10, 32), (10, 40, 16)], [(0, 2, 32), (2, 40, 16)]),  # C = 256
+    (12, 300, 12, 64, None, None),                       # C = 768: bytes only
+    (4, 100, 3, 344, [(0, 4, 16)], [(0, 4, 16)]),        # C = 1032: not a multiple of 32
+    (3, 77, 1, 64, [(0, 3, 16)], [(0, 3, 8)]),           # C = 64: row groups of 2 channels
+])
+def test_workspace_layout(L, T, H, D, k, v):
+    """The workspace is the status block, per-tile totals and bases, the
+    symbol scratch (one region of T rows per K/V layer pair; 16-bin pairs keep
+    4-bit codes when the encoder counts four channels per thread and C is a
+    multiple of 32) and one slot of C + 32 bytes per stream."""
+    if k is None:
+        k, v = cg.preset_specs(L)
+    C = H * D
+    plan = cg.cg_plan_create(L, T, H, D, 256, k, v)
+    try:
+        s = cg.cg_plan_sizes(plan)
+        up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+        tiles = s.num_tiles
+        w = up(256 + 4 * tiles)
+        w = up(w + 8 * (tiles + 1))
+        bins = [b for specs in (k, v) for (a, e, b) in specs for _ in range(a, e)]
+        nib = _count_layout(C, 16)[0] == 4 and C % 32 == 0
+        row_bytes = sum(C // 2 if (nib and b == 16) else C for b in bins)
+        w = up(w + T * row_bytes)
+        w = up(w + 2 * L * T * ((C + 32 + 15) // 16 * 16))
+        assert s.workspace_bytes == w
+    finally:
+        cg.cg_plan_destroy(plan)
