@@ -1466,7 +1466,11 @@ __device__ __forceinline__ void dec_start(DecState &st, const Bits &br)
 
 // Decode the next C symbols of a stream with the CDF rows of `table` (row c
 // for the c-th of them) and write their dequantised values to orow[0, C).
-template <int NB, int R>
+// WIDE (16 and 32 bins): the search probes three candidates per level (a
+// 4-way split; 2 levels for 16 bins, 2 + a last binary one for 32) instead
+// of one: more instructions but half the dependent shared-memory round
+// trips, for calls with too few streams to hide latency.
+template <int NB, int R, bool WIDE = false>
 __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t *table, int32_t C,
                                                    int32_t N, float a, const float *deq,
                                                    uint16_t *orow)
@@ -1489,7 +1493,21 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
             // probe is then base + offset + constant)
             const char *rb = reinterpret_cast<const char *>(row);
             uint32_t sb = 0;
-            if (NB > 0 && (NB & (NB - 1)) == 0) {
+            if (WIDE && (NB == 16 || NB == 32)) {
+                // levels of quarter steps q: candidates sb + q, + 2q, + 3q
+#pragma unroll
+                for (uint32_t q = (uint32_t)NB / 4; q >= 1; q /= 4) {
+                    const uint32_t e1 = *reinterpret_cast<const uint16_t *>(rb + sb + 2 * q);
+                    const uint32_t e2 = *reinterpret_cast<const uint16_t *>(rb + sb + 4 * q);
+                    const uint32_t e3 = *reinterpret_cast<const uint16_t *>(rb + sb + 6 * q);
+                    const bool p1 = scale16(d, e1) <= v, p2 = scale16(d, e2) <= v;
+                    const bool p3 = scale16(d, e3) <= v;
+                    sb += p3 ? 6 * q : p2 ? 4 * q : p1 ? 2 * q : 0u;
+                }
+                if (NB == 32 &&
+                    scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) <= v)
+                    sb += 2;
+            } else if (NB > 0 && (NB & (NB - 1)) == 0) {
 #pragma unroll
                 for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
                     if (scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step)) <= v)
@@ -1554,14 +1572,14 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
 // short of bits (the output is then wrong and the caller decodes the stream
 // again with R = 1, which never runs short: a symbol takes at most 18 bits
 // and the buffer holds at least 33 after every refill).
-template <int NB, int R>
+template <int NB, int R, bool WIDE = false>
 __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t C, int32_t N,
                                                   const Bits &br, float a, const float *deq,
                                                   uint16_t *orow)
 {
     DecState st;
     dec_start(st, br);
-    return decode_symbols<NB, R>(st, table, C, N, a, deq, orow);
+    return decode_symbols<NB, R, WIDE>(st, table, C, N, a, deq, orow);
 }
 
 // The refill-per-symbol decode of one stream, out of line: it runs only for
@@ -1655,7 +1673,7 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
     uint16_t *orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + sidx) * (size_t)C;
     Bits br;
     bits_init(br, bytestream, sb, last);
-    if (decode_stream<NB, kRefillEvery>(table, C, N, br, a, deq, orow))
+    if (decode_stream<NB, kRefillEvery, (NTH < NT)>(table, C, N, br, a, deq, orow))
         decode_stream_exact<NB>(table, C, N, bytestream, sb, last, a, deq, orow);
 }
 
@@ -1736,7 +1754,8 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
         }
         if (active) {
             const DecState saved = st;
-            if (decode_symbols<NB, kRefillEvery>(st, table, nch, N, a, deq, orow + c_begin)) {
+            if (decode_symbols<NB, kRefillEvery, (NTH < NT)>(st, table, nch, N, a, deq,
+                                                             orow + c_begin)) {
                 st = saved;
                 decode_part_exact<NB>(&st, table, nch, N, a, deq, orow + c_begin);
             }
