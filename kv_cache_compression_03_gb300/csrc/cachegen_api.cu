@@ -193,6 +193,7 @@ cg_status cg_plan_create(const cg_config *cfg, cg_plan **plan_out)
     tp.T = T;
     tp.C = C;
     tp.chunk_tokens = ch;
+    tp.one = 1;
     tp.groups_per_object = (ch + CG_GROUP_TOKENS - 1) / CG_GROUP_TOKENS;
     tp.full_objects = T / ch;
     const int32_t tail = T - tp.full_objects * ch;

@@ -1421,15 +1421,18 @@ __device__ __forceinline__ void bits_skip(Bits &r, uint32_t S)
 
 // Refill for the batched loop below: avail may have gone negative there (a
 // batch needed more bits than were buffered; that stream is decoded again),
-// so both shifts clamp.
-__device__ __forceinline__ void bits_refill_clamped(Bits &r)
+// so both shifts clamp. nw holds the word at r.pos as loaded (byte order not
+// yet swapped); the load of the following one is issued here, a refill
+// ahead of its use.
+__device__ __forceinline__ void bits_refill_next(Bits &r, uint32_t &nw)
 {
     if (r.avail <= 32) {
-        const uint32_t w = bits_word(r);
+        const uint32_t w = __byte_perm(nw, 0, 0x0123);
         r.b1 |= __funnelshift_rc(w, 0u, (uint32_t)r.avail);        // w >> avail
         r.b0 = __funnelshift_lc(0u, w, (uint32_t)(32 - r.avail));  // w << (32 - avail)
         r.pos += 4;
         r.avail += 32;
+        nw = *reinterpret_cast<const uint32_t *>(r.base + min(r.pos, r.lim));
     }
 }
 
@@ -1440,6 +1443,60 @@ __device__ __forceinline__ void bits_refill_clamped(Bits &r)
 // does run short is detected (the count of buffered bits goes negative) and
 // the stream is decoded again refilling after every symbol.
 constexpr int kRefillEvery = 4;
+
+// Search target. The decoder wants the largest s with floor(r * cdf[s] /
+// 2^16) <= v (r = d + 1, the coder's own comparison). As cdf[s] < 2^16 that
+// holds exactly when cdf[s] <= T = floor(((v + 1) 2^16 - 1) / r), so one
+// target per symbol replaces a 64-bit product per probe. The estimate below
+// is round(v 2^16 / r) from d >> 9 and v >> 9 (made floats through the
+// exponent field: mad.hi gives 2^23 + x as bits, on the FMA pipe) and an
+// approximate reciprocal; for a valid stream (r > 2^30) it is T or T + 1.
+// The caller checks the symbol found against the exact bounds and searches
+// again with the exact comparison when they disagree, so any error in the
+// estimate costs time, never a wrong symbol.
+__device__ __forceinline__ uint32_t search_target(uint32_t d, uint32_t v)
+{
+    uint32_t db, vb;
+    asm("mad.hi.u32 %0, %1, 8388608, 1258291200;" : "=r"(db) : "r"(d));  // 0x4B000000 + (d >> 9)
+    asm("mad.hi.u32 %0, %1, 8388608, 1258291200;" : "=r"(vb) : "r"(v));
+    float rc;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(__uint_as_float(db) - 8388608.0f));
+    // + 1.5 * 2^23 puts the rounded quotient in the low mantissa bits
+    const float y = __fmaf_rn(__uint_as_float(vb) - 8388608.0f, rc * 65536.0f, 12582912.0f);
+    return __float_as_uint(y) - 0x4B400000u;
+}
+
+// sb += inc when e <= T. `one` is 1 but comes from the kernel's arguments,
+// so the predicated add compiles to a multiply-add on the FMA pipe and stays
+// off the integer ALU pipe, the decoder's busiest.
+__device__ __forceinline__ void probe_add(uint32_t &sb, uint32_t e, uint32_t T, uint32_t one,
+                                          uint32_t inc)
+{
+    asm("{\n\t.reg .pred p;\n\tsetp.le.u32 p, %1, %2;\n\t@p mad.lo.u32 %0, %3, %4, %0;\n\t}"
+        : "+r"(sb)
+        : "r"(e), "r"(T), "r"(one), "r"(inc));
+}
+
+// One level of the search over positions sb/2 + q, + 2q, + 3q of a row
+// (rb: the row's bytes, sb: a byte offset, entries 2 bytes). The three
+// loads are independent; as the row rises, the number of entries <= T is
+// the quarter to take.
+__device__ __forceinline__ void search_4way(uint32_t &sb, const char *rb, uint32_t q, uint32_t T,
+                                            uint32_t one)
+{
+    const uint32_t e1 = *reinterpret_cast<const uint16_t *>(rb + sb + 2 * q);
+    const uint32_t e2 = *reinterpret_cast<const uint16_t *>(rb + sb + 4 * q);
+    const uint32_t e3 = *reinterpret_cast<const uint16_t *>(rb + sb + 6 * q);
+    probe_add(sb, e1, T, one, 2 * q);
+    probe_add(sb, e2, T, one, 2 * q);
+    probe_add(sb, e3, T, one, 2 * q);
+}
+
+__device__ __forceinline__ void search_2way(uint32_t &sb, const char *rb, uint32_t q, uint32_t T,
+                                            uint32_t one)
+{
+    probe_add(sb, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * q), T, one, 2 * q);
+}
 
 // Decode one stream (C symbols with the CDF rows of `table`) and write its
 // dequantised row. R > 1 refills the bit buffer once per R symbols and
@@ -1466,21 +1523,28 @@ __device__ __forceinline__ void dec_start(DecState &st, const Bits &br)
 
 // Decode the next C symbols of a stream with the CDF rows of `table` (row c
 // for the c-th of them) and write their dequantised values to orow[0, C).
-// WIDE (16 and 32 bins): the search probes three candidates per level (a
-// 4-way split; 2 levels for 16 bins, 2 + a last binary one for 32) instead
-// of one: more instructions but half the dependent shared-memory round
-// trips, for calls with too few streams to hide latency.
+// For 16 and 32 bins the search compares against a target (search_target)
+// in levels of 4-way and binary steps: 16 bins one 4-way level (its loads
+// depend on nothing but the row, so they issue early) and two binary ones,
+// or with WIDE two 4-way levels (fewer dependent shared-memory round trips,
+// for calls with too few streams to hide latency); 32 bins two 4-way levels
+// and a binary one. `one` must be 1 (see probe_add).
 template <int NB, int R, bool WIDE = false>
 __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t *table, int32_t C,
                                                    int32_t N, float a, const float *deq,
-                                                   uint16_t *orow)
+                                                   uint16_t *orow, uint32_t one)
 {
+    constexpr bool TARGET = NB == 16 || NB == 32;
     const int32_t Lp = N + 1;
     uint32_t x = st.x, d = st.d, v = st.v;
     Bits br = st.br;
     const uint16_t *row = table;
     const uint32_t top_step = 1u << (31 - __clz((uint32_t)(N - 1)));
     uint32_t short_batch = 0;
+    // the next word of the stream, loaded one refill ahead
+    uint32_t nw = 0;
+    if (R > 1)
+        nw = *reinterpret_cast<const uint32_t *>(br.base + min(br.pos, br.lim));
 
     for (int32_t c0 = 0; c0 < C; c0 += 8) {
         uint32_t packed[4];
@@ -1493,20 +1557,21 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
             // probe is then base + offset + constant)
             const char *rb = reinterpret_cast<const char *>(row);
             uint32_t sb = 0;
-            if (WIDE && (NB == 16 || NB == 32)) {
-                // levels of quarter steps q: candidates sb + q, + 2q, + 3q
-#pragma unroll
-                for (uint32_t q = (uint32_t)NB / 4; q >= 1; q /= 4) {
-                    const uint32_t e1 = *reinterpret_cast<const uint16_t *>(rb + sb + 2 * q);
-                    const uint32_t e2 = *reinterpret_cast<const uint16_t *>(rb + sb + 4 * q);
-                    const uint32_t e3 = *reinterpret_cast<const uint16_t *>(rb + sb + 6 * q);
-                    const bool p1 = scale16(d, e1) <= v, p2 = scale16(d, e2) <= v;
-                    const bool p3 = scale16(d, e3) <= v;
-                    sb += p3 ? 6 * q : p2 ? 4 * q : p1 ? 2 * q : 0u;
+            if (TARGET) {
+                const uint32_t T = search_target(d, v);
+                if (NB == 16) {
+                    search_4way(sb, rb, 4, T, one);
+                    if (WIDE) {
+                        search_4way(sb, rb, 1, T, one);
+                    } else {
+                        search_2way(sb, rb, 2, T, one);
+                        search_2way(sb, rb, 1, T, one);
+                    }
+                } else {
+                    search_4way(sb, rb, 8, T, one);
+                    search_4way(sb, rb, 2, T, one);
+                    search_2way(sb, rb, 1, T, one);
                 }
-                if (NB == 32 &&
-                    scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) <= v)
-                    sb += 2;
             } else if (NB > 0 && (NB & (NB - 1)) == 0) {
 #pragma unroll
                 for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
@@ -1524,10 +1589,18 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
             // never holds the top symbol N - 1 (never coded); a corrupt one
             // that reaches it gets cdf[N] (stored as 0) as its upper bound
             // and decodes to garbage, still inside the buffers.
-            const uint32_t c0v = *reinterpret_cast<const uint16_t *>(rb + sb);
-            const uint32_t c1v = *reinterpret_cast<const uint16_t *>(rb + sb + 2);
-            const uint32_t t0 = scale16(d, c0v);
-            const uint32_t dn = scale16(d, c1v) - t0 - 1u;
+            uint32_t t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
+            uint32_t dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
+            if (TARGET && v - t0 > dn) {
+                // the target missed a bound (rare): search with the exact compare
+                sb = 0;
+#pragma unroll 1
+                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
+                    if (scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step)) <= v)
+                        sb += 2 * step;
+                t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
+                dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
+            }
             // renormalise (see Enc); v takes S new bits
             const uint32_t xs = x + t0;
             const uint32_t S = renorm_shift(xs, dn);
@@ -1542,7 +1615,7 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
                 br.avail -= (int32_t)S;
                 if ((j % R) == R - 1) {
                     short_batch |= (br.avail < 0) ? 1u : 0u;
-                    bits_refill_clamped(br);
+                    bits_refill_next(br, nw);
                 }
             }
             // dequantise: bf16(fp32((q - MAX) / MAX) * a), two values per
@@ -1575,11 +1648,11 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
 template <int NB, int R, bool WIDE = false>
 __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t C, int32_t N,
                                                   const Bits &br, float a, const float *deq,
-                                                  uint16_t *orow)
+                                                  uint16_t *orow, uint32_t one)
 {
     DecState st;
     dec_start(st, br);
-    return decode_symbols<NB, R, WIDE>(st, table, C, N, a, deq, orow);
+    return decode_symbols<NB, R, WIDE>(st, table, C, N, a, deq, orow, one);
 }
 
 // The refill-per-symbol decode of one stream, out of line: it runs only for
@@ -1588,11 +1661,11 @@ template <int NB>
 __device__ __noinline__ void decode_stream_exact(const uint16_t *table, int32_t C, int32_t N,
                                                  const uint8_t *bytestream, uint64_t sb,
                                                  uint64_t last, float a, const float *deq,
-                                                 uint16_t *orow)
+                                                 uint16_t *orow, uint32_t one)
 {
     Bits br;
     bits_init(br, bytestream, sb, last);
-    decode_stream<NB, 1>(table, C, N, br, a, deq, orow);
+    decode_stream<NB, 1>(table, C, N, br, a, deq, orow, one);
 }
 
 // The same for the symbols of one channel part, from the state `st` held
@@ -1600,10 +1673,10 @@ __device__ __noinline__ void decode_stream_exact(const uint16_t *table, int32_t 
 template <int NB>
 __device__ __noinline__ void decode_part_exact(DecState *st, const uint16_t *table, int32_t C,
                                                int32_t N, float a, const float *deq,
-                                               uint16_t *orow)
+                                               uint16_t *orow, uint32_t one)
 {
     DecState s = *st;
-    decode_symbols<NB, 1>(s, table, C, N, a, deq, orow);
+    decode_symbols<NB, 1>(s, table, C, N, a, deq, orow, one);
     *st = s;
 }
 
@@ -1673,8 +1746,8 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
     uint16_t *orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + sidx) * (size_t)C;
     Bits br;
     bits_init(br, bytestream, sb, last);
-    if (decode_stream<NB, kRefillEvery, (NTH < NT)>(table, C, N, br, a, deq, orow))
-        decode_stream_exact<NB>(table, C, N, bytestream, sb, last, a, deq, orow);
+    if (decode_stream<NB, kRefillEvery, (NTH < NT)>(table, C, N, br, a, deq, orow, P.one))
+        decode_stream_exact<NB>(table, C, N, bytestream, sb, last, a, deq, orow, P.one);
 }
 
 // One tile of the decoder whose CDF table is staged in channel parts of
@@ -1755,9 +1828,9 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
         if (active) {
             const DecState saved = st;
             if (decode_symbols<NB, kRefillEvery, (NTH < NT)>(st, table, nch, N, a, deq,
-                                                             orow + c_begin)) {
+                                                             orow + c_begin, P.one)) {
                 st = saved;
-                decode_part_exact<NB>(&st, table, nch, N, a, deq, orow + c_begin);
+                decode_part_exact<NB>(&st, table, nch, N, a, deq, orow + c_begin, P.one);
             }
         }
         __syncthreads();  // the next part overwrites the table

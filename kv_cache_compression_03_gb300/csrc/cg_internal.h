@@ -39,7 +39,8 @@ struct cg_tile_params {
     // symbols as 4-bit codes (C/2 bytes per token), all others as bytes; the
     // pairs' regions follow the order of `order`, each T rows long
     int32_t nib_begin, nib_end;
-    uint32_t pad_;
+    uint32_t one;  // always 1: a multiplier the decoder's compiler cannot fold
+                   // away (its search additions then run on the FMA pipe)
     uint8_t bins[2][CG_MAX_LAYERS];
     uint32_t cdf_off[2][CG_MAX_LAYERS];  // offset of (kv, l) inside a group block
     // (kv, layer) pairs as (kv << 8) | layer, largest bin count first: the
