@@ -1521,20 +1521,37 @@ __device__ __forceinline__ void dec_start(DecState &st, const Bits &br)
     bits_skip(st.br, 16);
 }
 
+// The largest s in [0, N - 1) with floor(r * cdf[s] / 2^16) <= v by the
+// coder's own comparison (the byte offset 2s; NB = 0: any N, top_step the
+// largest power of two below N).
+template <int NB>
+__device__ __forceinline__ uint32_t exact_search(const char *rb, uint32_t d, uint32_t v, int32_t N,
+                                                 uint32_t top_step)
+{
+    uint32_t sb = 0;
+#pragma unroll 1
+    for (uint32_t step = NB > 0 ? (uint32_t)NB / 2 : top_step; step != 0; step >>= 1) {
+        const uint32_t t = sb + 2 * step;
+        if ((NB > 0 || t < 2 * (uint32_t)N) &&
+            scale16(d, *reinterpret_cast<const uint16_t *>(rb + t)) <= v)
+            sb = t;
+    }
+    return sb;
+}
+
 // Decode the next C symbols of a stream with the CDF rows of `table` (row c
 // for the c-th of them) and write their dequantised values to orow[0, C).
-// For 16 and 32 bins the search compares against a target (search_target)
-// in levels of 4-way and binary steps: 16 bins one 4-way level (its loads
-// depend on nothing but the row, so they issue early) and two binary ones,
-// or with WIDE two 4-way levels (fewer dependent shared-memory round trips,
-// for calls with too few streams to hide latency); 32 bins two 4-way levels
-// and a binary one. `one` must be 1 (see probe_add).
+// The search compares against a target (search_target): 16 bins in one
+// 4-way level (its loads depend on nothing but the row, so they issue
+// early) and two binary ones, or with WIDE two 4-way levels (fewer
+// dependent shared-memory round trips, for calls with too few streams to
+// hide latency); 32 bins in two 4-way levels and a binary one; other counts
+// (NB = 0) in binary steps. `one` must be 1 (see probe_add).
 template <int NB, int R, bool WIDE = false>
 __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t *table, int32_t C,
                                                    int32_t N, float a, const float *deq,
                                                    uint16_t *orow, uint32_t one)
 {
-    constexpr bool TARGET = NB == 16 || NB == 32;
     const int32_t Lp = N + 1;
     uint32_t x = st.x, d = st.d, v = st.v;
     Bits br = st.br;
@@ -1557,31 +1574,23 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
             // probe is then base + offset + constant)
             const char *rb = reinterpret_cast<const char *>(row);
             uint32_t sb = 0;
-            if (TARGET) {
-                const uint32_t T = search_target(d, v);
-                if (NB == 16) {
-                    search_4way(sb, rb, 4, T, one);
-                    if (WIDE) {
-                        search_4way(sb, rb, 1, T, one);
-                    } else {
-                        search_2way(sb, rb, 2, T, one);
-                        search_2way(sb, rb, 1, T, one);
-                    }
+            const uint32_t T = search_target(d, v);
+            if (NB == 16) {
+                search_4way(sb, rb, 4, T, one);
+                if (WIDE) {
+                    search_4way(sb, rb, 1, T, one);
                 } else {
-                    search_4way(sb, rb, 8, T, one);
-                    search_4way(sb, rb, 2, T, one);
+                    search_2way(sb, rb, 2, T, one);
                     search_2way(sb, rb, 1, T, one);
                 }
-            } else if (NB > 0 && (NB & (NB - 1)) == 0) {
-#pragma unroll
-                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
-                    if (scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step)) <= v)
-                        sb += 2 * step;
+            } else if (NB == 32) {
+                search_4way(sb, rb, 8, T, one);
+                search_4way(sb, rb, 2, T, one);
+                search_2way(sb, rb, 1, T, one);
             } else {
                 for (uint32_t step = top_step; step != 0; step >>= 1) {
                     const uint32_t t = sb + 2 * step;
-                    if (t < 2 * (uint32_t)N &&
-                        scale16(d, *reinterpret_cast<const uint16_t *>(rb + t)) <= v)
+                    if (t < 2 * (uint32_t)N && *reinterpret_cast<const uint16_t *>(rb + t) <= T)
                         sb = t;
                 }
             }
@@ -1591,13 +1600,9 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
             // and decodes to garbage, still inside the buffers.
             uint32_t t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
             uint32_t dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
-            if (TARGET && v - t0 > dn) {
+            if (v - t0 > dn) {
                 // the target missed a bound (rare): search with the exact compare
-                sb = 0;
-#pragma unroll 1
-                for (uint32_t step = (uint32_t)NB / 2; step != 0; step >>= 1)
-                    if (scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * step)) <= v)
-                        sb += 2 * step;
+                sb = exact_search<NB>(rb, d, v, N, top_step);
                 t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
                 dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
             }
