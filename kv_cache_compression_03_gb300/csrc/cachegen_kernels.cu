@@ -1547,11 +1547,16 @@ __device__ __forceinline__ uint32_t exact_search(const char *rb, uint32_t d, uin
 // dependent shared-memory round trips, for calls with too few streams to
 // hide latency); 32 bins in two 4-way levels and a binary one; other counts
 // (NB = 0) in binary steps. `one` must be 1 (see probe_add).
-template <int NB, int R, bool WIDE = false>
+// Output: KB symbols per store, 16 (one 32-byte store, a whole DRAM sector;
+// C a multiple of 16 and orow 32-byte aligned) or 8 (16 bytes). A sector
+// written in two halves some symbols apart is merged in L2, which fills
+// from DRAM the halves it evicts before they are complete.
+template <int NB, int R, bool WIDE = false, int KB = 8>
 __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t *table, int32_t C,
                                                    int32_t N, float a, const float *deq,
                                                    uint16_t *orow, uint32_t one)
 {
+    static_assert(KB == 8 || KB == 16, "8 or 16 symbols per store");
     const int32_t Lp = N + 1;
     uint32_t x = st.x, d = st.d, v = st.v;
     Bits br = st.br;
@@ -1563,80 +1568,90 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
     if (R > 1)
         nw = *reinterpret_cast<const uint32_t *>(br.base + min(br.pos, br.lim));
 
-    for (int32_t c0 = 0; c0 < C; c0 += 8) {
-        uint32_t packed[4];
-        float y_even = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's
-            // own comparison, so the result is exact)
-            // (sb = 2s, the position as a byte offset into the row: every
-            // probe is then base + offset + constant)
-            const char *rb = reinterpret_cast<const char *>(row);
-            uint32_t sb = 0;
-            const uint32_t T = search_target(d, v);
-            if (NB == 16) {
-                search_4way(sb, rb, 4, T, one);
-                if (WIDE) {
-                    search_4way(sb, rb, 1, T, one);
-                } else {
-                    search_2way(sb, rb, 2, T, one);
-                    search_2way(sb, rb, 1, T, one);
-                }
-            } else if (NB == 32) {
-                search_4way(sb, rb, 8, T, one);
-                search_4way(sb, rb, 2, T, one);
+    // one symbol (j: its place in the block, for the refill cadence);
+    // returns its dequantised value
+    auto symbol = [&](int j) -> float {
+        // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's own
+        // comparison, so the result is exact); sb = 2s, the position as a
+        // byte offset into the row: every probe is then base + offset +
+        // constant
+        const char *rb = reinterpret_cast<const char *>(row);
+        uint32_t sb = 0;
+        const uint32_t T = search_target(d, v);
+        if (NB == 16) {
+            search_4way(sb, rb, 4, T, one);
+            if (WIDE) {
+                search_4way(sb, rb, 1, T, one);
+            } else {
+                search_2way(sb, rb, 2, T, one);
                 search_2way(sb, rb, 1, T, one);
-            } else {
-                for (uint32_t step = top_step; step != 0; step >>= 1) {
-                    const uint32_t t = sb + 2 * step;
-                    if (t < 2 * (uint32_t)N && *reinterpret_cast<const uint16_t *>(rb + t) <= T)
-                        sb = t;
-                }
             }
-            // sb <= 2(N - 1), so both bounds lie in the row. A valid stream
-            // never holds the top symbol N - 1 (never coded); a corrupt one
-            // that reaches it gets cdf[N] (stored as 0) as its upper bound
-            // and decodes to garbage, still inside the buffers.
-            uint32_t t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
-            uint32_t dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
-            if (v - t0 > dn) {
-                // the target missed a bound (rare): search with the exact compare
-                sb = exact_search<NB>(rb, d, v, N, top_step);
-                t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
-                dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
+        } else if (NB == 32) {
+            search_4way(sb, rb, 8, T, one);
+            search_4way(sb, rb, 2, T, one);
+            search_2way(sb, rb, 1, T, one);
+        } else {
+            for (uint32_t step = top_step; step != 0; step >>= 1) {
+                const uint32_t t = sb + 2 * step;
+                if (t < 2 * (uint32_t)N && *reinterpret_cast<const uint16_t *>(rb + t) <= T)
+                    sb = t;
             }
-            // renormalise (see Enc); v takes S new bits
-            const uint32_t xs = x + t0;
-            const uint32_t S = renorm_shift(xs, dn);
-            x = shl_clamped(xs, S);
-            d = __funnelshift_l(0xFFFFFFFFu, dn, S);
-            v = __funnelshift_l(br.b1, v - t0, S);
-            if (R == 1) {
-                bits_skip(br, S);
-            } else {
-                br.b1 = __funnelshift_l(br.b0, br.b1, S);
-                br.b0 = shl_clamped(br.b0, S);
-                br.avail -= (int32_t)S;
-                if ((j % R) == R - 1) {
-                    short_batch |= (br.avail < 0) ? 1u : 0u;
-                    bits_refill_next(br, nw);
-                }
-            }
-            // dequantise: bf16(fp32((q - MAX) / MAX) * a), two values per
-            // conversion (each rounded to nearest even on its own)
-            const float y =
-                __fmul_rn(*reinterpret_cast<const float *>(reinterpret_cast<const char *>(deq) + 2 * sb), a);
-            if (j & 1) {
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(y_even, y);
-                packed[j >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
-            } else {
-                y_even = y;
-            }
-            row += Lp;
         }
-        *reinterpret_cast<uint4 *>(orow + c0) =
-            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        // sb <= 2(N - 1), so both bounds lie in the row. A valid stream never
+        // holds the top symbol N - 1 (never coded); a corrupt one that reaches
+        // it gets cdf[N] (stored as 0) as its upper bound and decodes to
+        // garbage, still inside the buffers.
+        uint32_t t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
+        uint32_t dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
+        if (v - t0 > dn) {
+            // the target missed a bound (rare): search with the exact compare
+            sb = exact_search<NB>(rb, d, v, N, top_step);
+            t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
+            dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
+        }
+        // renormalise (see Enc); v takes S new bits
+        const uint32_t xs = x + t0;
+        const uint32_t S = renorm_shift(xs, dn);
+        x = shl_clamped(xs, S);
+        d = __funnelshift_l(0xFFFFFFFFu, dn, S);
+        v = __funnelshift_l(br.b1, v - t0, S);
+        if (R == 1) {
+            bits_skip(br, S);
+        } else {
+            br.b1 = __funnelshift_l(br.b0, br.b1, S);
+            br.b0 = shl_clamped(br.b0, S);
+            br.avail -= (int32_t)S;
+            if ((j % R) == R - 1) {
+                short_batch |= (br.avail < 0) ? 1u : 0u;
+                bits_refill_next(br, nw);
+            }
+        }
+        row += Lp;
+        // dequantise: fp32((q - MAX) / MAX) * a
+        return __fmul_rn(*reinterpret_cast<const float *>(reinterpret_cast<const char *>(deq) + 2 * sb), a);
+    };
+    // two values per bf16 conversion (each rounded to nearest even on its own)
+    auto pack = [](float lo, float hi) -> uint32_t {
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&pr);
+    };
+
+    for (int32_t c0 = 0; c0 < C; c0 += KB) {
+        uint32_t p[KB / 2];
+#pragma unroll
+        for (int j = 0; j < KB; j += 2) {
+            const float lo = symbol(j);
+            p[j >> 1] = pack(lo, symbol(j + 1));
+        }
+        if (KB == 16)
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                         :
+                         : "l"(orow + c0), "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]),
+                           "r"(p[4 % (KB / 2)]), "r"(p[5 % (KB / 2)]), "r"(p[6 % (KB / 2)]),
+                           "r"(p[7 % (KB / 2)])
+                         : "memory");
+        else
+            *reinterpret_cast<uint4 *>(orow + c0) = make_uint4(p[0], p[1], p[2], p[3]);
     }
     st.x = x;
     st.d = d;
@@ -1650,14 +1665,14 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
 // short of bits (the output is then wrong and the caller decodes the stream
 // again with R = 1, which never runs short: a symbol takes at most 18 bits
 // and the buffer holds at least 33 after every refill).
-template <int NB, int R, bool WIDE = false>
+template <int NB, int R, bool WIDE = false, int KB = 8>
 __device__ __forceinline__ uint32_t decode_stream(const uint16_t *table, int32_t C, int32_t N,
                                                   const Bits &br, float a, const float *deq,
                                                   uint16_t *orow, uint32_t one)
 {
     DecState st;
     dec_start(st, br);
-    return decode_symbols<NB, R, WIDE>(st, table, C, N, a, deq, orow, one);
+    return decode_symbols<NB, R, WIDE, KB>(st, table, C, N, a, deq, orow, one);
 }
 
 // The refill-per-symbol decode of one stream, out of line: it runs only for
@@ -1686,8 +1701,8 @@ __device__ __noinline__ void decode_part_exact(DecState *st, const uint16_t *tab
 }
 
 // One tile of the decoder; NB as in encode_tile. The CTA takes streams
-// [h * NTH, (h + 1) * NTH) of the tile.
-template <int NB, int NTH>
+// [h * NTH, (h + 1) * NTH) of the tile; KB as in decode_symbols.
+template <int NB, int NTH, int KB>
 __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params &P,
                                             const uint8_t *__restrict__ bytestream,
                                             uint64_t stream_bytes,
@@ -1751,7 +1766,7 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
     uint16_t *orow = kv_out + ((size_t)(tl.l * 2 + tl.kv) * P.T + tl.t0 + sidx) * (size_t)C;
     Bits br;
     bits_init(br, bytestream, sb, last);
-    if (decode_stream<NB, kRefillEvery, (NTH < NT)>(table, C, N, br, a, deq, orow, P.one))
+    if (decode_stream<NB, kRefillEvery, (NTH < NT), KB>(table, C, N, br, a, deq, orow, P.one))
         decode_stream_exact<NB>(table, C, N, bytestream, sb, last, a, deq, orow, P.one);
 }
 
@@ -1762,7 +1777,7 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
 // staying in registers; a block barrier separates the parts. A stream whose
 // batched decode of a part ran short of bits decodes that part again, from
 // the state it held at the part's start, refilling after every symbol.
-template <int NB, int NTH>
+template <int NB, int NTH, int KB>
 __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_params &P,
                                                   const uint8_t *__restrict__ bytestream,
                                                   uint64_t stream_bytes,
@@ -1832,8 +1847,8 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
         }
         if (active) {
             const DecState saved = st;
-            if (decode_symbols<NB, kRefillEvery, (NTH < NT)>(st, table, nch, N, a, deq,
-                                                             orow + c_begin, P.one)) {
+            if (decode_symbols<NB, kRefillEvery, (NTH < NT), KB>(st, table, nch, N, a, deq,
+                                                                 orow + c_begin, P.one)) {
                 st = saved;
                 decode_part_exact<NB>(&st, table, nch, N, a, deq, orow + c_begin, P.one);
             }
@@ -1845,8 +1860,9 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
 // Decoder tiles of one launch class (NB bins; 0 = any), at least MINB
 // 256-thread CTAs' worth per SM; PARTS: the CDF table is staged in parts of
 // part_ch channels; NTH < 256: each tile's streams are split over 256 / NTH
-// CTAs of NTH threads (for calls with too few tiles to fill the GPU).
-template <int NB, int MINB, bool PARTS, int NTH>
+// CTAs of NTH threads (for calls with too few tiles to fill the GPU); KB:
+// symbols per output store (decode_symbols).
+template <int NB, int MINB, bool PARTS, int NTH, int KB = 8>
 __global__ void __launch_bounds__(NTH, MINB *(NT / NTH))
     k_decode_class(const cg_tile_params P, int32_t cls_begin,
                    const uint8_t *__restrict__ bytestream, uint64_t stream_bytes,
@@ -1863,10 +1879,10 @@ __global__ void __launch_bounds__(NTH, MINB *(NT / NTH))
     const Tile tl = tile_of_class(P, cls_begin, blockIdx.x / split);
     const int32_t h = (int32_t)(blockIdx.x % split);
     if (PARTS)
-        decode_tile_parts<NB, NTH>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
+        decode_tile_parts<NB, NTH, KB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
                                    kv_out, status, smem, warp_sums, deq, &bad, part_ch, h, offs);
     else
-        decode_tile<NB, NTH>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
+        decode_tile<NB, NTH, KB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
                              kv_out, status, smem, warp_sums, deq, &bad, h, offs);
 }
 
@@ -1901,25 +1917,28 @@ bool encode_groups(int32_t C, int32_t bins)
     return r > 1;
 }
 
-template <int NTH>
+template <int NTH, int KB>
 decode_fn decode_kernel_nth(int32_t bins, bool parts)
 {
     if (bins == 16)
-        return parts ? k_decode_class<16, 4, true, NTH>
-                     : k_decode_class<16, (NTH == NT ? 6 : 4), false, NTH>;
+        return parts ? k_decode_class<16, 4, true, NTH, KB>
+                     : k_decode_class<16, (NTH == NT ? 6 : 4), false, NTH, KB>;
     if (bins == 32)
-        return parts ? k_decode_class<32, 4, true, NTH> : k_decode_class<32, 3, false, NTH>;
-    return parts ? k_decode_class<0, 4, true, NTH> : k_decode_class<0, 3, false, NTH>;
+        return parts ? k_decode_class<32, 4, true, NTH, KB> : k_decode_class<32, 3, false, NTH, KB>;
+    return parts ? k_decode_class<0, 4, true, NTH, KB> : k_decode_class<0, 3, false, NTH, KB>;
 }
 
-// split: CTAs per tile (1, 2 or 4)
-decode_fn decode_kernel(int32_t bins, bool parts, int split)
+// split: CTAs per tile (1, 2 or 4); sectors: every row (or row part) the
+// launch writes is a whole number of 32-byte sectors at a 32-byte aligned
+// address, for 32-byte output stores (one CTA per tile only: the split
+// kernels, for small calls, keep 16-byte stores)
+decode_fn decode_kernel(int32_t bins, bool parts, int split, bool sectors)
 {
     if (split == 4)
-        return decode_kernel_nth<NT / 4>(bins, parts);
+        return decode_kernel_nth<NT / 4, 8>(bins, parts);
     if (split == 2)
-        return decode_kernel_nth<NT / 2>(bins, parts);
-    return decode_kernel_nth<NT>(bins, parts);
+        return decode_kernel_nth<NT / 2, 8>(bins, parts);
+    return sectors ? decode_kernel_nth<NT, 16>(bins, parts) : decode_kernel_nth<NT, 8>(bins, parts);
 }
 
 // Number of SMs of the current device.
@@ -1954,9 +1973,10 @@ cudaError_t ensure_smem_attributes()
                                        CG_SMEM_LIMIT - 2048);
         for (int parts = 0; parts < 2 && err == cudaSuccess; ++parts)
             for (int split = 1; split <= 4 && err == cudaSuccess; split *= 2)
-                err = cudaFuncSetAttribute(decode_kernel(bins[i], parts != 0, split),
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           CG_SMEM_LIMIT - 2048);
+                for (int sectors = 0; sectors < 2 && err == cudaSuccess; ++sectors)
+                    err = cudaFuncSetAttribute(decode_kernel(bins[i], parts != 0, split, sectors != 0),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               CG_SMEM_LIMIT - 2048);
     }
     if (err == cudaSuccess)
         done.fetch_or(bit);
@@ -2172,8 +2192,10 @@ cudaError_t cg_launch_decode(const cg_plan *p, const cg_encoded *in, uint64_t st
     const int split = ((int64_t)ntiles * 2 < (int64_t)sms * 3) ? 4 : 1;
     err = launch_classes(p, stream, [&](const cg_bin_class &cl, cudaStream_t s) {
         const int32_t part_ch = cg_decode_part_channels(p->C, cl.bins);
-        decode_kernel(cl.bins, part_ch < p->C, split)<<<p->tp.ngroups * cl.count * split,
-                                                        NT / split, cl.smem_decode, s>>>(
+        const bool sectors = p->C % 16 == 0 && part_ch % 16 == 0 &&
+                             reinterpret_cast<uintptr_t>(kv_out) % 32 == 0;
+        decode_kernel(cl.bins, part_ch < p->C, split, sectors)<<<
+            p->tp.ngroups * cl.count * split, NT / split, cl.smem_decode, s>>>(
             p->tp, cl.begin, in->bytestream, stream_bytes, in->lengths, in->cdf, in->amax,
             tile_base, static_cast<uint16_t *>(kv_out), status, part_ch);
     });

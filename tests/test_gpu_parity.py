@@ -211,6 +211,32 @@ def test_repeatable_and_side_stream(orc):
     assert np.array_equal(_bits(out).reshape(L, 2, T, C), orc.decode(ref, L, T, C, 256, k, v))
 
 
+@pytest.mark.parametrize("name,T", [("mistral7b_t1k", 300), ("llama8b_t16k", 300)])
+def test_decode_into_an_output_aligned_to_16_bytes_only(orc, name, T):
+    """The decoder writes 32-byte sectors when the output allows it; an
+    output that starts 16 bytes past a 32-byte boundary takes the kernels
+    with 16-byte stores (llama: 16-bin tiles and 32-bin tiles in channel
+    parts). Both must give the oracle's bytes."""
+    p = synthetic.WORKLOADS[name]
+    bits = synthetic.generate(name, num_tokens=T)
+    k, v = synthetic.workload_specs(name)
+    L, _, T, C = bits.shape
+    codec = cg.Codec(L, T, p["H"], p["D"], 256, k, v)
+    enc = codec.encode(_to_dev(bits, p["H"], p["D"]))
+    n = L * 2 * T * C
+    buf = torch.empty(n + 32, dtype=torch.bfloat16, device="cuda")
+    off = ((32 - buf.data_ptr() % 32) % 32 + 16) // 2
+    out = buf[off:off + n].view(L, 2, T, p["H"], p["D"])
+    assert out.data_ptr() % 32 == 16
+    codec.decode(enc, kv_out=out)
+    ref = orc.encode(bits, 256, k, v)
+    want = orc.decode(ref, L, T, C, 256, k, v)
+    assert np.array_equal(_bits(out).reshape(L, 2, T, C), want)
+    aligned = codec.decode(enc)
+    assert aligned.data_ptr() % 32 == 0
+    assert np.array_equal(_bits(aligned).reshape(L, 2, T, C), want)
+
+
 def test_nonfinite_input_is_reported():
     name = "opt125m_t256"
     p = synthetic.WORKLOADS[name]
