@@ -36,12 +36,14 @@
 // copies four streams at a time from their slots to their packed position.
 // Decode: per tile, the CDF block (or one channel part at a time) is
 // staged in shared memory, the lengths are scanned, and each thread decodes
-// one stream (binary search with the coder's exact comparison; the bit
-// buffer refilled once per kRefillEvery symbols) and writes the
-// dequantised bf16 row; calls with few tiles split each tile's streams over
-// four CTAs. A stream (or part) whose batch of symbols over- or under-runs
-// the 64-bit bit buffer (possible only for runs of a group's rarest
-// symbols) is redone on an exact path that checks after every symbol.
+// one stream (a search of the CDF row against a per-symbol target, checked
+// against the coder's exact bounds; the bit buffer refilled once per
+// kRefillEvery symbols) and writes the dequantised bf16 row, 16 symbols per
+// 32-byte store where the rows allow it; calls with few tiles split each
+// tile's streams over four CTAs. A stream (or part) whose batch of symbols
+// over- or under-runs the 64-bit bit buffer (possible only for runs of a
+// group's rarest symbols) is redone on an exact path that checks after
+// every symbol.
 //
 // No kernel waits on another block, and every loop is bounded by the
 // tile's token and channel counts or the alphabet size.
