@@ -36,21 +36,14 @@ def _digest() -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libcachegen.so (if stale) and return its path."""
-    os.makedirs(OUT_DIR, exist_ok=True)
-    stamp = os.path.join(OUT_DIR, "libcachegen.stamp")
-    dig = _digest()
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
-        with open(stamp) as f:
-            if f.read().strip() == dig:
-                return LIB
+def _compile(out_dir: str, lib: str, defines=()) -> str:
     nvcc = _nvcc()
+    extra = ["-D" + d for d in defines]
     procs, objs = [], []
     for s in SOURCES:
-        obj = os.path.join(OUT_DIR, s.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, s.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [nvcc] + ARCH + FLAGS + ["-c", os.path.join(CSRC, s), "-o", obj]
+        cmd = [nvcc] + ARCH + FLAGS + extra + ["-c", os.path.join(CSRC, s), "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
                                             text=True)))
     log = []
@@ -59,19 +52,44 @@ def build(force: bool = False, verbose: bool = False) -> str:
         log.append(out)
         if p.returncode != 0:
             raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + out)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     link = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
-    with open(os.path.join(OUT_DIR, "ptxas.log"), "w") as f:
+    os.replace(tmp, lib)
+    with open(os.path.join(out_dir, "ptxas.log"), "w") as f:
         f.write("\n".join(log))
+    return "\n".join(log)
+
+
+def _build_into(out_dir: str, defines=(), force: bool = False, verbose: bool = False) -> str:
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(out_dir, "libcachegen.so")
+    stamp = os.path.join(out_dir, "libcachegen.stamp")
+    dig = _digest() + " " + " ".join(defines)
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == dig:
+                return lib
+    log = _compile(out_dir, lib, defines)
     with open(stamp, "w") as f:
         f.write(dig)
     if verbose:
-        sys.stdout.write("\n".join(log))
-    return LIB
+        sys.stdout.write(log)
+    return lib
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libcachegen.so (if stale) and return its path."""
+    return _build_into(OUT_DIR, (), force, verbose)
+
+
+def build_test_variant(name: str, defines) -> str:
+    """A library compiled with test-only macros (cachegen_kernels.cu names
+    them: each forces one of the rarely taken exact paths), in
+    _build/<name>/. For the tests; the product library never sets them."""
+    return _build_into(os.path.join(OUT_DIR, name), tuple(defines))
 
 
 if __name__ == "__main__":

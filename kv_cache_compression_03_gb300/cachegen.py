@@ -13,6 +13,7 @@ first 2 V layers use 32 bins, the rest 16; fewer than 10 layers: all 32).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as ct
 import os
 import threading
@@ -76,47 +77,66 @@ def load(build_if_missing: bool = True) -> ct.CDLL:
         if build_if_missing:
             from . import build as _build
             path = _build.build()
-        if not os.path.exists(path):
-            raise ImportError(f"libcachegen.so not found at {path}; run build() first")
-        L = ct.CDLL(path)
-        P, sz, u64 = ct.c_void_p, ct.c_size_t, ct.c_uint64
-        st = ct.c_int
-        sigs = {
-            "cg_plan_create": (st, [ct.POINTER(cg_config), ct.POINTER(ct.c_void_p)]),
-            "cg_plan_destroy": (None, [P]),
-            "cg_plan_sizes": (st, [P, ct.POINTER(cg_sizes)]),
-            "cg_plan_config": (st, [P, ct.POINTER(cg_config), ct.POINTER(cg_quant_spec),
-                                    ct.c_int32, ct.POINTER(cg_quant_spec), ct.c_int32]),
-            "cg_encode": (st, [P, P, P, sz, ct.POINTER(cg_encoded), P]),
-            "cg_decode": (st, [P, ct.POINTER(cg_encoded), u64, P, sz, P, P]),
-            "cg_last_device_error": (st, [P, P, ct.POINTER(ct.c_int), ct.POINTER(u64), P]),
-            "cg_container_size": (st, [P, u64, ct.POINTER(sz)]),
-            "cg_serialize": (st, [P, ct.POINTER(cg_encoded), u64, P, sz, ct.POINTER(sz), P]),
-            "cg_container_open": (st, [P, sz, ct.POINTER(ct.c_void_p), ct.POINTER(u64)]),
-            "cg_deserialize": (st, [P, P, sz, ct.POINTER(cg_encoded), P]),
-            "cg_status_string": (ct.c_char_p, [st]),
-            "cg_encode_noalloc": (st, [P, P, ct.POINTER(cg_encoded), P, P]),
-            "cg_object_range": (st, [P, ct.c_int32, ct.POINTER(ct.c_int32),
-                                     ct.POINTER(ct.c_int32)]),
-            "cg_object_streams": (st, [P, P, ct.c_int32, ct.POINTER(u64), ct.POINTER(u64), P]),
-            "cg_object_container_size": (st, [P, ct.c_int32, u64, ct.POINTER(sz)]),
-            "cg_serialize_object": (st, [P, ct.POINTER(cg_encoded), P, ct.c_int32, P, sz,
-                                         ct.POINTER(sz), P]),
-            "cg_deserialize_objects": (st, [P, ct.c_int32, ct.POINTER(ct.c_void_p),
-                                            ct.POINTER(sz), ct.POINTER(cg_encoded),
-                                            ct.POINTER(u64), P]),
-            "cg_int8_encode": (st, [P, ct.c_int64, ct.c_int32, P, P, P, P]),
-            "cg_int8_decode": (st, [P, P, ct.c_int64, ct.c_int32, P, P]),
-            "cg_profile_enable": (st, [P, ct.c_int32]),
-            "cg_profile_read": (st, [P, ct.POINTER(cg_kernel_profile), ct.c_int32,
-                                     ct.POINTER(ct.c_int32)]),
-        }
-        for name, (res, args) in sigs.items():
-            f = getattr(L, name)
-            f.restype = res
-            f.argtypes = args
-        _lib = L
-        return L
+        _lib = _open(path)
+        return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Run the calls of this module against another build of the library
+    (the tests' variants with forced slow paths), then switch back."""
+    global _lib
+    L = _open(path)
+    with _lock:
+        prev, _lib = _lib, L
+    try:
+        yield L
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def _open(path: str) -> ct.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libcachegen.so not found at {path}; run build() first")
+    L = ct.CDLL(path)
+    P, sz, u64 = ct.c_void_p, ct.c_size_t, ct.c_uint64
+    st = ct.c_int
+    sigs = {
+        "cg_plan_create": (st, [ct.POINTER(cg_config), ct.POINTER(ct.c_void_p)]),
+        "cg_plan_destroy": (None, [P]),
+        "cg_plan_sizes": (st, [P, ct.POINTER(cg_sizes)]),
+        "cg_plan_config": (st, [P, ct.POINTER(cg_config), ct.POINTER(cg_quant_spec),
+                                ct.c_int32, ct.POINTER(cg_quant_spec), ct.c_int32]),
+        "cg_encode": (st, [P, P, P, sz, ct.POINTER(cg_encoded), P]),
+        "cg_decode": (st, [P, ct.POINTER(cg_encoded), u64, P, sz, P, P]),
+        "cg_last_device_error": (st, [P, P, ct.POINTER(ct.c_int), ct.POINTER(u64), P]),
+        "cg_container_size": (st, [P, u64, ct.POINTER(sz)]),
+        "cg_serialize": (st, [P, ct.POINTER(cg_encoded), u64, P, sz, ct.POINTER(sz), P]),
+        "cg_container_open": (st, [P, sz, ct.POINTER(ct.c_void_p), ct.POINTER(u64)]),
+        "cg_deserialize": (st, [P, P, sz, ct.POINTER(cg_encoded), P]),
+        "cg_status_string": (ct.c_char_p, [st]),
+        "cg_encode_noalloc": (st, [P, P, ct.POINTER(cg_encoded), P, P]),
+        "cg_object_range": (st, [P, ct.c_int32, ct.POINTER(ct.c_int32),
+                                 ct.POINTER(ct.c_int32)]),
+        "cg_object_streams": (st, [P, P, ct.c_int32, ct.POINTER(u64), ct.POINTER(u64), P]),
+        "cg_object_container_size": (st, [P, ct.c_int32, u64, ct.POINTER(sz)]),
+        "cg_serialize_object": (st, [P, ct.POINTER(cg_encoded), P, ct.c_int32, P, sz,
+                                     ct.POINTER(sz), P]),
+        "cg_deserialize_objects": (st, [P, ct.c_int32, ct.POINTER(ct.c_void_p),
+                                        ct.POINTER(sz), ct.POINTER(cg_encoded),
+                                        ct.POINTER(u64), P]),
+        "cg_int8_encode": (st, [P, ct.c_int64, ct.c_int32, P, P, P, P]),
+        "cg_int8_decode": (st, [P, P, ct.c_int64, ct.c_int32, P, P]),
+        "cg_profile_enable": (st, [P, ct.c_int32]),
+        "cg_profile_read": (st, [P, ct.POINTER(cg_kernel_profile), ct.c_int32,
+                                 ct.POINTER(ct.c_int32)]),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
 
 
 def _check(st: int, what: str):

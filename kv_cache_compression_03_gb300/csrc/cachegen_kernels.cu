@@ -47,6 +47,13 @@
 //
 // No kernel waits on another block, and every loop is bounded by the
 // tile's token and channel counts or the alphabet size.
+//
+// Test builds only (the product library defines neither): with
+// CG_TEST_TARGET_MISS every decoder search target misses, so each symbol
+// above the lowest takes the exact re-search; with CG_TEST_EXACT_PATHS the
+// encoder codes every stream (and, with channel parts, every part after the
+// first) again on its exact path and the decoder decodes every stream (or
+// part) again refilling after every symbol. Outputs must not change.
 
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -1098,6 +1105,9 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
             uint32_t wp = 0, flag = 0;
             uint32_t bits = nib ? code_stream<false, true>(srow, C, table, Lp, out, cap, &wp, &flag)
                                 : code_stream<false, false>(srow, C, table, Lp, out, cap, &wp, &flag);
+#ifdef CG_TEST_EXACT_PATHS
+            flag = 1;
+#endif
             if (flag) {
                 const uint64_t r = nib ? code_stream_exact<true>(srow, C, table, Lp, out, cap)
                                        : code_stream_exact<false>(srow, C, table, Lp, out, cap);
@@ -1167,6 +1177,10 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
                         code_symbols<false, false>(e, srow, c_begin, nch, table, Lp);
                     if (last)
                         bits = enc_finish<false>(e);
+#ifdef CG_TEST_EXACT_PATHS
+                    if (c_begin > 0)
+                        e.flag = 1;
+#endif
                     if (e.flag) {
                         e = save;
                         exact = true;
@@ -1465,6 +1479,9 @@ __device__ __forceinline__ uint32_t search_target(uint32_t d, uint32_t v)
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(__uint_as_float(db) - 8388608.0f));
     // + 1.5 * 2^23 puts the rounded quotient in the low mantissa bits
     const float y = __fmaf_rn(__uint_as_float(vb) - 8388608.0f, rc * 65536.0f, 12582912.0f);
+#ifdef CG_TEST_TARGET_MISS
+    return 0u * __float_as_uint(y);
+#endif
     return __float_as_uint(y) - 0x4B400000u;
 }
 
@@ -1659,6 +1676,10 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
     st.d = d;
     st.v = v;
     st.br = br;
+#ifdef CG_TEST_EXACT_PATHS
+    if (R > 1)
+        short_batch = 1;
+#endif
     return short_batch;
 }
 
