@@ -67,7 +67,7 @@ def _build_into(out_dir: str, defines=(), force: bool = False, verbose: bool = F
     os.makedirs(out_dir, exist_ok=True)
     lib = os.path.join(out_dir, "libcachegen.so")
     stamp = os.path.join(out_dir, "libcachegen.stamp")
-    dig = _digest() + " " + " ".join(defines)
+    dig = " ".join([_digest()] + list(defines))
     if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == dig:
