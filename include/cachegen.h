@@ -110,7 +110,8 @@ typedef enum cg_status {
     CG_ERR_NONFINITE = 4,   /* the input holds inf or NaN, or a row too
                                small for a finite scale factor */
     CG_ERR_CORRUPT = 5,     /* a container or its tables are inconsistent */
-    CG_ERR_TIMEOUT = 6,     /* reserved: a bounded device wait gave up */
+    CG_ERR_TIMEOUT = 6,     /* a bounded device wait gave up (the decoder's
+                               wait for a CDF table's bulk copy) */
     CG_ERR_CUDA = 7,        /* a CUDA runtime call failed */
     CG_ERR_UNSUPPORTED = 8  /* the shape exceeds this build's limits */
 } cg_status;

@@ -73,6 +73,80 @@ __device__ __forceinline__ void set_status(uint32_t *st, uint32_t code)
     atomicCAS(st, 0u, code);
 }
 
+// ------------------------------------------------------------ bulk copies
+// A tile's CDF rows reach shared memory in one bulk copy (cp.async.bulk:
+// the TMA engine, no tensor map) that completes on a shared-memory
+// mbarrier, so the CTA's threads do other work meanwhile. Thread 0 issues
+// the copy; every thread that reads the table waits on the barrier's phase.
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// thread 0, then a block barrier before the first use
+__device__ __forceinline__ void mbar_init(uint64_t *bar)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Thread 0: copy `bytes` (a multiple of 16) from src (16-byte aligned) to
+// dst; completes the barrier's current phase. Earlier reads of dst by the
+// block must be ordered before this (a block barrier): the proxy fence then
+// orders them before the copy's writes.
+__device__ __forceinline__ void bulk_copy_to_smem(void *dst, const void *src, uint32_t bytes,
+                                                  uint64_t *bar)
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Wait until the barrier completes the phase of the given parity; false if
+// it has not after kWaitLimit polls (each poll may suspend the thread for a
+// while), so a copy that never lands cannot hang the kernel.
+constexpr uint32_t kWaitLimit = 1u << 20;
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (done)
+            return true;
+    }
+    return false;
+}
+
+// Stage a table of `bytes` from src into dst: one bulk copy when src and
+// bytes are 16-byte multiples (always, for CDF blocks of a valid plan),
+// else a plain copy by all NTH threads (then complete after the caller's
+// next block barrier). Returns whether the barrier must be waited on.
+template <int NTH>
+__device__ __forceinline__ bool stage_table(uint16_t *dst, const uint16_t *src, uint32_t bytes,
+                                            uint64_t *bar)
+{
+    if (((reinterpret_cast<uintptr_t>(src) | bytes) & 15u) == 0) {
+        if (threadIdx.x == 0)
+            bulk_copy_to_smem(dst, src, bytes, bar);
+        return true;
+    }
+    for (uint32_t i = threadIdx.x; i < bytes / 2; i += NTH)
+        dst[i] = src[i];
+    return false;
+}
+
 struct Tile {
     int32_t index;  // (g * 2 + kv) * L + l
     int32_t g, kv, l, t0, n, N;
@@ -1736,7 +1810,7 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
                                             uint16_t *__restrict__ kv_out,
                                             uint32_t *__restrict__ status, uint8_t *smem,
                                             uint32_t *warp_sums, float *deq, uint32_t *bad,
-                                            int32_t h, uint32_t *offs)
+                                            int32_t h, uint32_t *offs, uint64_t *bar)
 {
     const int32_t C = P.C;
     const int32_t N = NB > 0 ? NB : tl.N;
@@ -1746,19 +1820,19 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
     const int32_t sidx = h * NTH + tid;
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
 
-    if (tid == 0)
+    if (tid == 0) {
         *bad = 0;
-    {
-        const uint32_t nb16 = (uint32_t)C * Lp * 2u / 16u;
-        const uint4 *src = reinterpret_cast<const uint4 *>(cdf + tl.cdf_base);
-        uint4 *dst = reinterpret_cast<uint4 *>(table);
-        for (uint32_t i = tid; i < nb16; i += NTH)
-            dst[i] = __ldg(src + i);
+        mbar_init(bar);
     }
+    __syncthreads();
+    // the table's bulk copy runs while the lengths are scanned
+    const bool bulk = stage_table<NTH>(table, cdf + tl.cdf_base, (uint32_t)C * Lp * 2u, bar);
     if (tid < N)
         deq[tid] = __fdiv_rn((float)(tid - M), (float)M);
     uint32_t len = 0;
     const uint32_t off = tile_stream_offset<NTH>(tl, lengths, h, &len, warp_sums, offs);
+    if (bulk && !mbar_wait(bar, 0))
+        *bad = 2;
     // every row must start at 0, rise strictly and end at 65536 (stored 0)
     for (int32_t c = tid; c < C; c += NTH) {
         const uint16_t *row = table + (size_t)c * Lp;
@@ -1766,12 +1840,14 @@ __device__ __forceinline__ void decode_tile(const Tile &tl, const cg_tile_params
         for (int32_t i = 1; i < N; ++i)
             ok &= (row[i] > row[i - 1]) ? 1u : 0u;
         if (!ok)
-            *bad = 1;
+            atomicMax(bad, 1u);
     }
     __syncthreads();
     if (*bad) {
         if (tid == 0)
-            set_status(status, CG_ERR_CORRUPT);
+            set_status(status, *bad == 2 ? CG_ERR_TIMEOUT : CG_ERR_CORRUPT);
+        if (*bad == 2)
+            mbar_wait(bar, 0);  // one more bounded wait for the copy in flight
         return;
     }
     if (sidx >= tl.n)
@@ -1811,7 +1887,8 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
                                                   uint16_t *__restrict__ kv_out,
                                                   uint32_t *__restrict__ status, uint8_t *smem,
                                                   uint32_t *warp_sums, float *deq, uint32_t *bad,
-                                                  int32_t part_ch, int32_t h, uint32_t *offs)
+                                                  int32_t part_ch, int32_t h, uint32_t *offs,
+                                                  uint64_t *bar)
 {
     const int32_t C = P.C;
     const int32_t N = NB > 0 ? NB : tl.N;
@@ -1821,8 +1898,13 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
     const int32_t sidx = h * NTH + tid;
     uint16_t *table = reinterpret_cast<uint16_t *>(smem);
 
-    if (tid == 0)
+    if (tid == 0) {
         *bad = 0;
+        mbar_init(bar);
+    }
+    __syncthreads();
+    // the first part's bulk copy runs while the lengths are scanned
+    bool bulk = stage_table<NTH>(table, cdf + tl.cdf_base, (uint32_t)min(part_ch, C) * Lp * 2u, bar);
     if (tid < N)
         deq[tid] = __fdiv_rn((float)(tid - M), (float)M);
     uint32_t len = 0;
@@ -1844,28 +1926,32 @@ __device__ __forceinline__ void decode_tile_parts(const Tile &tl, const cg_tile_
         bits_init(br, bytestream, sb, last);
         dec_start(st, br);
     }
-    for (int32_t c_begin = 0; c_begin < C; c_begin += part_ch) {
+    uint32_t phase = 0;
+    for (int32_t c_begin = 0; c_begin < C; c_begin += part_ch, phase ^= 1u) {
         const int32_t nch = min(part_ch, C - c_begin);
-        {
-            const uint32_t nb16 = (uint32_t)nch * Lp * 2u / 16u;
-            const uint4 *src = reinterpret_cast<const uint4 *>(cdf + tl.cdf_base + (size_t)c_begin * Lp);
-            uint4 *dst = reinterpret_cast<uint4 *>(table);
-            for (uint32_t i = tid; i < nb16; i += NTH)
-                dst[i] = __ldg(src + i);
+        if (c_begin > 0)  // after the block barrier that ends the previous part
+            bulk = stage_table<NTH>(table, cdf + tl.cdf_base + (size_t)c_begin * Lp,
+                                    (uint32_t)nch * Lp * 2u, bar);
+        if (bulk) {
+            if (!mbar_wait(bar, phase))
+                *bad = 2;
+        } else {
+            __syncthreads();  // the plain copy is complete
         }
-        __syncthreads();
         for (int32_t c = tid; c < nch; c += NTH) {
             const uint16_t *row = table + (size_t)c * Lp;
             uint32_t ok = (row[0] == 0) && (row[N] == 0);
             for (int32_t i = 1; i < N; ++i)
                 ok &= (row[i] > row[i - 1]) ? 1u : 0u;
             if (!ok)
-                *bad = 1;
+                atomicMax(bad, 1u);
         }
         __syncthreads();
         if (*bad) {
             if (tid == 0)
-                set_status(status, CG_ERR_CORRUPT);
+                set_status(status, *bad == 2 ? CG_ERR_TIMEOUT : CG_ERR_CORRUPT);
+            if (*bad == 2)
+                mbar_wait(bar, phase);  // one more bounded wait for the copy in flight
             return;
         }
         if (active) {
@@ -1898,15 +1984,17 @@ __global__ void __launch_bounds__(NTH, MINB *(NT / NTH))
     __shared__ float deq[64];
     __shared__ uint32_t bad;
     __shared__ uint32_t offs[NTH < NT ? NT : 1];
+    __shared__ uint64_t bar;
     constexpr int split = NT / NTH;
     const Tile tl = tile_of_class(P, cls_begin, blockIdx.x / split);
     const int32_t h = (int32_t)(blockIdx.x % split);
     if (PARTS)
         decode_tile_parts<NB, NTH, KB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
-                                   kv_out, status, smem, warp_sums, deq, &bad, part_ch, h, offs);
+                                   kv_out, status, smem, warp_sums, deq, &bad, part_ch, h, offs,
+                                   &bar);
     else
         decode_tile<NB, NTH, KB>(tl, P, bytestream, stream_bytes, lengths, cdf, amax, tile_base,
-                             kv_out, status, smem, warp_sums, deq, &bad, h, offs);
+                             kv_out, status, smem, warp_sums, deq, &bad, h, offs, &bar);
 }
 
 // The kernel of each class, by bin count: 16 and 32 have specialised
