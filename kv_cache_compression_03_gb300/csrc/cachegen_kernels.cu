@@ -53,7 +53,10 @@
 // above the lowest takes the exact re-search; with CG_TEST_EXACT_PATHS the
 // encoder codes every stream (and, with channel parts, every part after the
 // first) again on its exact path and the decoder decodes every stream (or
-// part) again refilling after every symbol. Outputs must not change.
+// part) again refilling after every symbol. Outputs must not change. With
+// CG_TEST_WAIT_TIMEOUT each table copy's barrier expects 16 bytes more than
+// the copy brings (the copy itself completes), so the decoder's bounded
+// wait runs out and the call reports CG_ERR_TIMEOUT.
 
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -98,9 +101,14 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar)
 __device__ __forceinline__ void bulk_copy_to_smem(void *dst, const void *src, uint32_t bytes,
                                                   uint64_t *bar)
 {
+#ifdef CG_TEST_WAIT_TIMEOUT
+    const uint32_t expect = bytes + 16u;  // a phase that never completes
+#else
+    const uint32_t expect = bytes;
+#endif
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
+                 "r"(expect)
                  : "memory");
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
@@ -112,7 +120,11 @@ __device__ __forceinline__ void bulk_copy_to_smem(void *dst, const void *src, ui
 // Wait until the barrier completes the phase of the given parity; false if
 // it has not after kWaitLimit polls (each poll may suspend the thread for a
 // while), so a copy that never lands cannot hang the kernel.
+#ifdef CG_TEST_WAIT_TIMEOUT
+constexpr uint32_t kWaitLimit = 1u << 12;
+#else
 constexpr uint32_t kWaitLimit = 1u << 20;
+#endif
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     for (uint32_t i = 0; i < kWaitLimit; ++i) {

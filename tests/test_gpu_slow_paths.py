@@ -74,3 +74,24 @@ def test_forced_exact_paths_match_the_oracle(orc, variant, name, T, chunk, specs
         assert np.array_equal(enc.bytestream[:enc.stream_bytes].cpu().numpy(), ref["bytes"])
         assert np.array_equal(_bits(out).reshape(L, 2, T, C), want)
         del codec, enc, out
+
+
+def test_a_decoder_wait_that_runs_out_is_reported(orc):
+    """The decoder's wait for its table copy is bounded: in a build whose
+    barrier expects 16 bytes more than the copy brings, the wait runs out,
+    the call reports CG_ERR_TIMEOUT and returns, and the context stays
+    usable (the product library then decodes the same streams exactly)."""
+    name, T = "mistral7b_t1k", 300
+    bits, H, D, k, v = _case(name, T, None)
+    L, _, T, C = bits.shape
+    codec = cg.Codec(L, T, H, D, 256, k, v)
+    enc = codec.encode(_to_dev(bits, H, D))
+    lib = build.build_test_variant("test_cg_test_wait_timeout", ["CG_TEST_WAIT_TIMEOUT"])
+    with cg.use_library(lib):
+        with pytest.raises(cg.CacheGenError) as e:
+            codec.decode(enc)
+        assert e.value.status == cg.CG_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    ref = orc.encode(bits, 256, k, v)
+    out = codec.decode(enc)
+    assert np.array_equal(_bits(out).reshape(L, 2, T, C), orc.decode(ref, L, T, C, 256, k, v))
