@@ -1550,21 +1550,17 @@ constexpr int kRefillEvery = 4;
 // 2^16) <= v (r = d + 1, the coder's own comparison). As cdf[s] < 2^16 that
 // holds exactly when cdf[s] <= T = floor(((v + 1) 2^16 - 1) / r), so one
 // target per symbol replaces a 64-bit product per probe. The estimate below
-// is round(v 2^16 / r) from d >> 9 and v >> 9 (made floats through the
-// exponent field: mad.hi gives 2^23 + x as bits, on the FMA pipe) and an
-// approximate reciprocal; for a valid stream (r > 2^30) it is T or T + 1.
-// The caller checks the symbol found against the exact bounds and searches
-// again with the exact comparison when they disagree, so any error in the
-// estimate costs time, never a wrong symbol.
+// is round(v 2^16 / r) from d and v converted to floats (rounded toward
+// zero) and an approximate reciprocal of d / 2^16; for a valid stream
+// (r > 2^30) it is T or T + 1. The caller checks the symbol found against
+// the exact bounds and searches again with the exact comparison when they
+// disagree, so any error in the estimate costs time, never a wrong symbol.
 __device__ __forceinline__ uint32_t search_target(uint32_t d, uint32_t v)
 {
-    uint32_t db, vb;
-    asm("mad.hi.u32 %0, %1, 8388608, 1258291200;" : "=r"(db) : "r"(d));  // 0x4B000000 + (d >> 9)
-    asm("mad.hi.u32 %0, %1, 8388608, 1258291200;" : "=r"(vb) : "r"(v));
     float rc;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(__uint_as_float(db) - 8388608.0f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(__uint2float_rz(d) * (1.0f / 65536.0f)));
     // + 1.5 * 2^23 puts the rounded quotient in the low mantissa bits
-    const float y = __fmaf_rn(__uint_as_float(vb) - 8388608.0f, rc * 65536.0f, 12582912.0f);
+    const float y = __fmaf_rn(__uint2float_rz(v), rc, 12582912.0f);
 #ifdef CG_TEST_TARGET_MISS
     return 0u * __float_as_uint(y);
 #endif
