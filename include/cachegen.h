@@ -182,10 +182,14 @@ cg_status cg_encode(const cg_plan *plan, const void *kv, void *workspace, size_t
  * stream_bytes bytes of streams; bytestream_capacity must be at least
  * stream_bytes rounded up to 16; stream_bytes below the number of
  * streams is CG_ERR_CORRUPT) into kv_out (device, bf16
- * [L][2][T][H*D], 16-byte aligned) [CG-LMCache §5]. Invalid CDF rows or
- * lengths that do not add up to stream_bytes set CG_ERR_CORRUPT on the
- * device; decoding of a corrupt stream still ends after C symbols per
- * stream and never reads outside the buffers. Asynchronous on stream. */
+ * [L][2][T][H*D], 16-byte aligned) [CG-LMCache §5]. With kv_out 32-byte
+ * aligned and H*D a multiple of 16 every row is written in whole 32-byte
+ * sectors (faster); otherwise in 16-byte pieces, with the same result.
+ * Invalid CDF rows or lengths that do not add up to stream_bytes set
+ * CG_ERR_CORRUPT on the device; a bounded wait inside the decoder that
+ * runs out sets CG_ERR_TIMEOUT. Decoding of a corrupt stream still ends
+ * after C symbols per stream and never reads outside the buffers.
+ * Asynchronous on stream. */
 cg_status cg_decode(const cg_plan *plan, const cg_encoded *in, uint64_t stream_bytes,
                     void *workspace, size_t workspace_bytes, void *kv_out, cg_stream_t stream);
 
