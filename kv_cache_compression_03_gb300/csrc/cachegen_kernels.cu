@@ -12,14 +12,18 @@
 // shared-memory size and CTAs per SM, and the launches of one call run
 // concurrently on the caller's stream and a forked side stream. Encode
 // (then a tile scan and a pack):
-//   A  blocks of 16 token rows: warp per row computes amax over the C
-//      channels (16-byte loads; |x| maximum on bf16 bit patterns, one warp
-//      reduction) and the row's scale factor; then a thread per four
-//      channels re-reads the block (L1/L2-resident), quantises (the
-//      rounding to an integer as an fp32 addition of 1.5 * 2^23), counts
-//      into its own shared-memory histogram rows (no atomics) and writes
-//      the symbols to a scratch row per stream (4-bit codes for 16 bins,
-//      else bytes). The next block's amax overlaps this block's counting.
+//   A  16-bin rows of 1024 channels: each thread loads its four channels of
+//      eight rows once (the next eight in flight), the row maxima are
+//      reduced across the block from those registers, and the same values
+//      are quantised (the rounding to an integer as an fp32 addition of
+//      1.5 * 2^23), counted into the thread's own shared-memory histogram
+//      rows (no atomics) and written to a scratch row per stream as 4-bit
+//      codes. Other rows, in blocks of 16: warp per row computes amax over
+//      the C channels (16-byte loads; |x| maximum on bf16 bit patterns, one
+//      warp reduction) and the row's scale factor; then a thread per four
+//      channels re-reads the block (L1/L2-resident), quantises, counts and
+//      writes the symbols (4-bit codes for 16 bins, else bytes). The next
+//      block's amax overlaps this block's counting.
 //      Rows under 1024 channels are counted by row groups, each group into
 //      its own histogram copy (cg_count_layout); at <= 512 channels the
 //      maxima of all rows come first and the counting runs without block
@@ -928,6 +932,76 @@ __device__ __forceinline__ void store_factors(int32_t ra, uint32_t ma, int32_t r
     }
 }
 
+// Phase A for 16-bin tiles of exactly 4 * NT channels (4-bit symbols): the
+// tile's raw data is read once. Thread p holds channels 4p..4p+3 of eight
+// rows in registers (the next eight rows' loads already in flight), the
+// row maxima are reduced across the block from those registers (a warp
+// reduction, then eight warp maxima per row), and the same registers are
+// then quantised and counted. Two block barriers per eight rows.
+template <int NB>
+__device__ __forceinline__ void count_tile_single_read(const uint16_t *__restrict__ rows,
+                                                       int32_t C, int32_t n, float fmax,
+                                                       float *fac, float *amax_row,
+                                                       uint32_t *nonfinite, uint16_t *table,
+                                                       int32_t N, uint8_t *sym_tile)
+{
+    __shared__ uint32_t wmax[NT / 32][8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t Lp = N + 1;
+    uint16_t *h0 = table + (size_t)(4 * tid) * Lp;
+    const uint2 *src = reinterpret_cast<const uint2 *>(rows) + tid;
+    uint2 w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        w[u] = (u < n) ? __ldg(src + (size_t)u * (C / 4)) : make_uint2(0u, 0u);
+    for (int32_t r0 = 0; r0 < n; r0 += 8) {
+        const int32_t nr = min(8, n - r0);
+        uint2 wn[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            wn[u] = (r0 + 8 + u < n) ? __ldg(src + (size_t)(r0 + 8 + u) * (C / 4))
+                                     : make_uint2(0u, 0u);
+        // |x| maxima on bf16 bit patterns: per thread, per warp, per row
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t m = __vmaxu2(w[u].x & 0x7FFF7FFFu, w[u].y & 0x7FFF7FFFu);
+            const uint32_t mw = absmax_reduce(m);
+            if (lane == 0)
+                wmax[warp][u] = mw;
+        }
+        __syncthreads();
+        if (tid < nr) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < NT / 32; ++i)
+                m = max(m, wmax[i][tid]);
+            fac[r0 + tid] = row_factor(m, fmax, nonfinite);
+            amax_row[r0 + tid] = __uint_as_float(m << 16);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (u < nr) {
+                const float f = fac[r0 + u];
+                const uint32_t q0 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x << 16), f, fmax), N);
+                const uint32_t q1 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x & 0xFFFF0000u), f, fmax), N);
+                const uint32_t q2 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y << 16), f, fmax), N);
+                const uint32_t q3 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y & 0xFFFF0000u), f, fmax), N);
+                h0[q0] += 1;
+                h0[Lp + q1] += 1;
+                h0[2 * Lp + q2] += 1;
+                h0[3 * Lp + q3] += 1;
+                reinterpret_cast<uint16_t *>(sym_tile)[tid + (size_t)(r0 + u) * (C / 4)] =
+                    (uint16_t)(q0 + 16u * q1 + 256u * q2 + 4096u * q3);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            w[u] = wn[u];
+    }
+    __syncthreads();  // every count is in before phase B reads the table
+}
+
 // Ask L2 for rows [r, r + nr) of the tile (one contiguous range).
 __device__ __forceinline__ void prefetch_rows(const uint16_t *rows, int32_t C, int32_t r,
                                               int32_t nr)
@@ -1099,6 +1173,9 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
             }
         }
         __syncthreads();
+    } else if (NB == 16 && !PARTS && nib && C == 4 * NT) {
+        count_tile_single_read<NB>(rows, C, tl.n, fmax, fac, amax_row, nonfinite, table, N,
+                                   sym_tile);
     } else {
     // A: amax of block 0; then per step, count block b while the loads for
     // block b + 1's amax are in flight (one row per warp), and ask L2 for
