@@ -1,6 +1,6 @@
 """Build the codec's shared library (libcachegen.so) in-tree with nvcc for
-sm_103a. The two translation units compile in parallel; the result is
-reused while the sources, headers and flags are unchanged."""
+sm_103a. The translation units compile in parallel; the result is reused
+while the sources, headers and flags are unchanged."""
 from __future__ import annotations
 
 import hashlib
@@ -87,8 +87,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 def build_test_variant(name: str, defines) -> str:
     """A library compiled with test-only macros (cachegen_kernels.cu names
-    them: each forces one of the rarely taken exact paths), in
-    _build/<name>/. For the tests; the product library never sets them."""
+    them: each forces a rarely taken path, an exact fallback or a bounded
+    wait that runs out), in _build/<name>/. For the tests; the product
+    library never sets them."""
     return _build_into(os.path.join(OUT_DIR, name), tuple(defines))
 
 
