@@ -12,10 +12,11 @@
 // shared-memory size and CTAs per SM, and the launches of one call run
 // concurrently on the caller's stream and a forked side stream. Encode
 // (then a tile scan and a pack):
-//   A  16-bin rows of 1024 channels: each thread loads its four channels of
-//      eight rows once (the next eight in flight), the row maxima are
-//      reduced across the block from those registers, and the same values
-//      are quantised (the rounding to an integer as an fp32 addition of
+//   A  16-bin rows counted four channels per thread whose row groups fill
+//      the block (1024 channels; 256 in four groups, ...): each thread loads
+//      its four channels of eight rows once (the next eight in flight), the
+//      row maxima are reduced across the block from those registers, and the
+//      same values are quantised (the rounding to an integer as an fp32 addition of
 //      1.5 * 2^23), counted into the thread's own shared-memory histogram
 //      rows (no atomics) and written to a scratch row per stream as 4-bit
 //      codes. Other rows, in blocks of 16: warp per row computes amax over
@@ -932,35 +933,44 @@ __device__ __forceinline__ void store_factors(int32_t ra, uint32_t ma, int32_t r
     }
 }
 
-// Phase A for 16-bin tiles of exactly 4 * NT channels (4-bit symbols): the
-// tile's raw data is read once. Thread p holds channels 4p..4p+3 of eight
-// rows in registers (the next eight rows' loads already in flight), the
-// row maxima are reduced across the block from those registers (a warp
-// reduction, then eight warp maxima per row), and the same registers are
-// then quantised and counted. Two block barriers per eight rows.
-template <int NB>
+// Phase A for 16-bin tiles counted four channels per thread with 4-bit
+// symbols, when R row groups of C/4 threads fill the block (C * R = 4 * NT:
+// 1024 channels with R = 1, 256 with R = 4, ...): the tile's raw data is
+// read once. Thread (g, p) of row group g holds channels 4p..4p+3 of rows
+// r0 + uR + g, u < 8, of each batch of 8R rows in registers (the next
+// batch's loads already in flight); the row maxima are reduced across the
+// block from those registers (a warp reduction, then the warp maxima of the
+// row's group), and the same registers are then quantised and counted into
+// the group's histogram copy. Two block barriers per batch.
+template <int NB, int R>
 __device__ __forceinline__ void count_tile_single_read(const uint16_t *__restrict__ rows,
                                                        int32_t C, int32_t n, float fmax,
                                                        float *fac, float *amax_row,
                                                        uint32_t *nonfinite, uint16_t *table,
                                                        int32_t N, uint8_t *sym_tile)
 {
+    constexpr int U = NT / R;      // threads per row group
+    constexpr int WPG = U / 32;    // warps per row group
+    static_assert(U % 32 == 0, "a row group is whole warps");
     __shared__ uint32_t wmax[NT / 32][8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = tid / U, p = tid % U;
     const int32_t Lp = N + 1;
-    uint16_t *h0 = table + (size_t)(4 * tid) * Lp;
-    const uint2 *src = reinterpret_cast<const uint2 *>(rows) + tid;
+    uint16_t *h0 = table + (size_t)g * C * Lp + (size_t)(4 * p) * Lp;
+    const uint2 *src = reinterpret_cast<const uint2 *>(rows) + p;
     uint2 w[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-        w[u] = (u < n) ? __ldg(src + (size_t)u * (C / 4)) : make_uint2(0u, 0u);
-    for (int32_t r0 = 0; r0 < n; r0 += 8) {
-        const int32_t nr = min(8, n - r0);
+    for (int u = 0; u < 8; ++u) {
+        const int32_t row = u * R + g;
+        w[u] = (row < n) ? __ldg(src + (size_t)row * (C / 4)) : make_uint2(0u, 0u);
+    }
+    for (int32_t r0 = 0; r0 < n; r0 += 8 * R) {
         uint2 wn[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            wn[u] = (r0 + 8 + u < n) ? __ldg(src + (size_t)(r0 + 8 + u) * (C / 4))
-                                     : make_uint2(0u, 0u);
+        for (int u = 0; u < 8; ++u) {
+            const int32_t row = r0 + 8 * R + u * R + g;
+            wn[u] = (row < n) ? __ldg(src + (size_t)row * (C / 4)) : make_uint2(0u, 0u);
+        }
         // |x| maxima on bf16 bit patterns: per thread, per warp, per row
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -970,19 +980,24 @@ __device__ __forceinline__ void count_tile_single_read(const uint16_t *__restric
                 wmax[warp][u] = mw;
         }
         __syncthreads();
-        if (tid < nr) {
-            uint32_t m = 0;
+        if (tid < 8 * R) {  // one thread per row of the batch
+            const int u = tid / R, gg = tid % R;
+            const int32_t row = r0 + u * R + gg;
+            if (row < n) {
+                uint32_t m = 0;
 #pragma unroll
-            for (int i = 0; i < NT / 32; ++i)
-                m = max(m, wmax[i][tid]);
-            fac[r0 + tid] = row_factor(m, fmax, nonfinite);
-            amax_row[r0 + tid] = __uint_as_float(m << 16);
+                for (int i = 0; i < WPG; ++i)
+                    m = max(m, wmax[gg * WPG + i][u]);
+                fac[row] = row_factor(m, fmax, nonfinite);
+                amax_row[row] = __uint_as_float(m << 16);
+            }
         }
         __syncthreads();
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            if (u < nr) {
-                const float f = fac[r0 + u];
+            const int32_t row = r0 + u * R + g;
+            if (row < n) {
+                const float f = fac[row];
                 const uint32_t q0 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x << 16), f, fmax), N);
                 const uint32_t q1 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].x & 0xFFFF0000u), f, fmax), N);
                 const uint32_t q2 = symbol_of<NB>(quantise_bits(__uint_as_float(w[u].y << 16), f, fmax), N);
@@ -991,7 +1006,7 @@ __device__ __forceinline__ void count_tile_single_read(const uint16_t *__restric
                 h0[Lp + q1] += 1;
                 h0[2 * Lp + q2] += 1;
                 h0[3 * Lp + q3] += 1;
-                reinterpret_cast<uint16_t *>(sym_tile)[tid + (size_t)(r0 + u) * (C / 4)] =
+                reinterpret_cast<uint16_t *>(sym_tile)[p + (size_t)row * (C / 4)] =
                     (uint16_t)(q0 + 16u * q1 + 256u * q2 + 4096u * q3);
             }
         }
@@ -1130,7 +1145,21 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
                         (uint64_t)tl.t0 * row_bytes;
     const int32_t nblocks = (tl.n + kRowsPerBlock - 1) / kRowsPerBlock;
 
-    if (GROUPS && C <= 512) {
+    if (NB == 16 && !PARTS && nib && cw == 4 && C * cr == 4 * NT) {
+        // 4-bit symbols, four channels per thread, the row groups fill the block
+        if (cr == 1)
+            count_tile_single_read<NB, 1>(rows, C, tl.n, fmax, fac, amax_row, nonfinite, table,
+                                          N, sym_tile);
+        else if (GROUPS && cr == 2)
+            count_tile_single_read<NB, 2>(rows, C, tl.n, fmax, fac, amax_row, nonfinite, table,
+                                          N, sym_tile);
+        else if (GROUPS && cr == 4)
+            count_tile_single_read<NB, 4>(rows, C, tl.n, fmax, fac, amax_row, nonfinite, table,
+                                          N, sym_tile);
+        else if (GROUPS && cr == 8)
+            count_tile_single_read<NB, 8>(rows, C, tl.n, fmax, fac, amax_row, nonfinite, table,
+                                          N, sym_tile);
+    } else if (GROUPS && C <= 512) {
         // A for rows of at most 512 channels counted by row groups (a tile of
         // at most 256 KB, which stays in L2 between the passes): the maxima
         // and factors of all rows first (a warp per two rows at a time), then
@@ -1173,9 +1202,6 @@ __device__ __forceinline__ void encode_tile(const Tile &tl, const uint16_t *__re
             }
         }
         __syncthreads();
-    } else if (NB == 16 && !PARTS && nib && C == 4 * NT) {
-        count_tile_single_read<NB>(rows, C, tl.n, fmax, fac, amax_row, nonfinite, table, N,
-                                   sym_tile);
     } else {
     // A: amax of block 0; then per step, count block b while the loads for
     // block b + 1's amax are in flight (one row per warp), and ask L2 for
