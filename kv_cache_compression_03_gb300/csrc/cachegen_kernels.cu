@@ -1654,20 +1654,38 @@ constexpr int kRefillEvery = 4;
 // holds exactly when cdf[s] <= T = floor(((v + 1) 2^16 - 1) / r), so one
 // target per symbol replaces a 64-bit product per probe. The estimate below
 // is round(v 2^16 / r) from d and v converted to floats (rounded toward
-// zero) and an approximate reciprocal of d / 2^16; for a valid stream
-// (r > 2^30) it is T or T + 1. The caller checks the symbol found against
-// the exact bounds and searches again with the exact comparison when they
-// disagree, so any error in the estimate costs time, never a wrong symbol.
+// zero) and an approximate reciprocal of d; for a valid stream (r > 2^30)
+// it is T or T + 1. The caller checks the symbol found against the exact
+// bounds and searches again with the exact comparison when they disagree, so
+// any error in the estimate costs time, never a wrong symbol.
 __device__ __forceinline__ uint32_t search_target(uint32_t d, uint32_t v)
 {
     float rc;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(__uint2float_rz(d) * (1.0f / 65536.0f)));
-    // + 1.5 * 2^23 puts the rounded quotient in the low mantissa bits
-    const float y = __fmaf_rn(__uint2float_rz(v), rc, 12582912.0f);
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(__uint2float_rz(d)));
+    // v / d < 4 even for a corrupt stream, so y stays in [128, 256), where
+    // the float spacing is 2^-16: adding 1.5 * 2^7 rounds v / d to a multiple
+    // of 2^-16, and the low mantissa bits of y are then round(v 2^16 / d)
+    const float y = __fmaf_rn(__uint2float_rz(v), rc, 192.0f);
 #ifdef CG_TEST_TARGET_MISS
     return 0u * __float_as_uint(y);
 #endif
-    return __float_as_uint(y) - 0x4B400000u;
+    return __float_as_uint(y) - 0x43400000u;  // the bits of 192.0f
+}
+
+// Shared-memory loads at 32-bit shared addresses (volatile: the decoder
+// stages a new table between calls in the channel-part kernels).
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a)
+{
+    uint32_t r;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(r) : "r"(a));
+    return r;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t a)
+{
+    float r;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(a));
+    return r;
 }
 
 // sb += inc when e <= T. `one` is 1 but comes from the kernel's arguments,
@@ -1681,25 +1699,24 @@ __device__ __forceinline__ void probe_add(uint32_t &sb, uint32_t e, uint32_t T, 
         : "r"(e), "r"(T), "r"(one), "r"(inc));
 }
 
-// One level of the search over positions sb/2 + q, + 2q, + 3q of a row
-// (rb: the row's bytes, sb: a byte offset, entries 2 bytes). The three
-// loads are independent; as the row rises, the number of entries <= T is
-// the quarter to take.
-__device__ __forceinline__ void search_4way(uint32_t &sb, const char *rb, uint32_t q, uint32_t T,
-                                            uint32_t one)
+// One level of the search at entries q, 2q and 3q above the current one
+// (p: its shared address; entries are 2 bytes). The three loads are
+// independent; as the row rises, the number of entries <= T is the quarter
+// to take. Tracking the address itself leaves every probe a load at p plus a
+// constant.
+__device__ __forceinline__ void search_4way(uint32_t &p, uint32_t q, uint32_t T, uint32_t one)
 {
-    const uint32_t e1 = *reinterpret_cast<const uint16_t *>(rb + sb + 2 * q);
-    const uint32_t e2 = *reinterpret_cast<const uint16_t *>(rb + sb + 4 * q);
-    const uint32_t e3 = *reinterpret_cast<const uint16_t *>(rb + sb + 6 * q);
-    probe_add(sb, e1, T, one, 2 * q);
-    probe_add(sb, e2, T, one, 2 * q);
-    probe_add(sb, e3, T, one, 2 * q);
+    const uint32_t e1 = lds_u16(p + 2 * q);
+    const uint32_t e2 = lds_u16(p + 4 * q);
+    const uint32_t e3 = lds_u16(p + 6 * q);
+    probe_add(p, e1, T, one, 2 * q);
+    probe_add(p, e2, T, one, 2 * q);
+    probe_add(p, e3, T, one, 2 * q);
 }
 
-__device__ __forceinline__ void search_2way(uint32_t &sb, const char *rb, uint32_t q, uint32_t T,
-                                            uint32_t one)
+__device__ __forceinline__ void search_2way(uint32_t &p, uint32_t q, uint32_t T, uint32_t one)
 {
-    probe_add(sb, *reinterpret_cast<const uint16_t *>(rb + sb + 2 * q), T, one, 2 * q);
+    probe_add(p, lds_u16(p + 2 * q), T, one, 2 * q);
 }
 
 // Decode one stream (C symbols with the CDF rows of `table`) and write its
@@ -1750,7 +1767,8 @@ __device__ __forceinline__ uint32_t exact_search(const char *rb, uint32_t d, uin
 // early) and two binary ones, or with WIDE two 4-way levels (fewer
 // dependent shared-memory round trips, for calls with too few streams to
 // hide latency); 32 bins in two 4-way levels and a binary one; other counts
-// (NB = 0) in binary steps. `one` must be 1 (see probe_add).
+// (NB = 0) in binary steps. `one` must be 1 (see probe_add); `table` and
+// `deq` are in shared memory.
 // Output: KB symbols per store, 16 (one 32-byte store, a whole DRAM sector;
 // C a multiple of 16 and orow 32-byte aligned) or 8 (16 bytes). A sector
 // written in two halves some symbols apart is merged in L2, which fills
@@ -1764,54 +1782,57 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
     const int32_t Lp = N + 1;
     uint32_t x = st.x, d = st.d, v = st.v;
     Bits br = st.br;
-    const uint16_t *row = table;
     const uint32_t top_step = 1u << (31 - __clz((uint32_t)(N - 1)));
     uint32_t short_batch = 0;
     // the next word of the stream, loaded one refill ahead
     uint32_t nw = 0;
     if (R > 1)
         nw = *reinterpret_cast<const uint32_t *>(br.base + min(br.pos, br.lim));
+    // shared addresses: r32 of the current symbol's CDF row, and kq with
+    // kq + 2 p = the dequantisation entry of the symbol whose lower bound
+    // sits at address p of that row
+    const uint32_t tab32 = smem_u32(table);
+    uint32_t r32 = tab32;
+    uint32_t kq = smem_u32(deq) - 2u * tab32;
 
     // one symbol (j: its place in the block, for the refill cadence);
     // returns its dequantised value
     auto symbol = [&](int j) -> float {
         // the largest s with floor(r * cdf[s] / 2^16) <= v (the coder's own
-        // comparison, so the result is exact); sb = 2s, the position as a
-        // byte offset into the row: every probe is then base + offset +
-        // constant
-        const char *rb = reinterpret_cast<const char *>(row);
-        uint32_t sb = 0;
+        // comparison, so the result is exact); p = the address of cdf[s]
+        uint32_t p = r32;
         const uint32_t T = search_target(d, v);
         if (NB == 16) {
-            search_4way(sb, rb, 4, T, one);
+            search_4way(p, 4, T, one);
             if (WIDE) {
-                search_4way(sb, rb, 1, T, one);
+                search_4way(p, 1, T, one);
             } else {
-                search_2way(sb, rb, 2, T, one);
-                search_2way(sb, rb, 1, T, one);
+                search_2way(p, 2, T, one);
+                search_2way(p, 1, T, one);
             }
         } else if (NB == 32) {
-            search_4way(sb, rb, 8, T, one);
-            search_4way(sb, rb, 2, T, one);
-            search_2way(sb, rb, 1, T, one);
+            search_4way(p, 8, T, one);
+            search_4way(p, 2, T, one);
+            search_2way(p, 1, T, one);
         } else {
             for (uint32_t step = top_step; step != 0; step >>= 1) {
-                const uint32_t t = sb + 2 * step;
-                if (t < 2 * (uint32_t)N && *reinterpret_cast<const uint16_t *>(rb + t) <= T)
-                    sb = t;
+                const uint32_t t = p + 2 * step;
+                if (t - r32 < 2 * (uint32_t)N && lds_u16(t) <= T)
+                    p = t;
             }
         }
-        // sb <= 2(N - 1), so both bounds lie in the row. A valid stream never
+        // s <= N - 1, so both bounds lie in the row. A valid stream never
         // holds the top symbol N - 1 (never coded); a corrupt one that reaches
         // it gets cdf[N] (stored as 0) as its upper bound and decodes to
         // garbage, still inside the buffers.
-        uint32_t t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
-        uint32_t dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
+        uint32_t t0 = scale16(d, lds_u16(p));
+        uint32_t dn = scale16(d, lds_u16(p + 2)) - t0 - 1u;
         if (v - t0 > dn) {
             // the target missed a bound (rare): search with the exact compare
-            sb = exact_search<NB>(rb, d, v, N, top_step);
-            t0 = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb));
-            dn = scale16(d, *reinterpret_cast<const uint16_t *>(rb + sb + 2)) - t0 - 1u;
+            const char *rb = reinterpret_cast<const char *>(table) + (r32 - tab32);
+            p = r32 + exact_search<NB>(rb, d, v, N, top_step);
+            t0 = scale16(d, lds_u16(p));
+            dn = scale16(d, lds_u16(p + 2)) - t0 - 1u;
         }
         // renormalise (see Enc); v takes S new bits
         const uint32_t xs = x + t0;
@@ -1830,9 +1851,12 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
                 bits_refill_next(br, nw);
             }
         }
-        row += Lp;
-        // dequantise: fp32((q - MAX) / MAX) * a
-        return __fmul_rn(*reinterpret_cast<const float *>(reinterpret_cast<const char *>(deq) + 2 * sb), a);
+        // dequantise: fp32((q - MAX) / MAX) * a, entry s of deq (4 bytes
+        // per entry, 2 per CDF entry)
+        const uint32_t qa = kq + 2u * p;
+        r32 += 2 * Lp;
+        kq -= 4 * Lp;
+        return __fmul_rn(lds_f32(qa), a);
     };
     // two values per bf16 conversion (each rounded to nearest even on its own)
     auto pack = [](float lo, float hi) -> uint32_t {
