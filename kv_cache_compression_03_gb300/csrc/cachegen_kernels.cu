@@ -1894,6 +1894,11 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
         return *reinterpret_cast<const uint32_t *>(&pr);
     };
 
+    // the output is written once and not read here: its stores allocate no
+    // L1 line and take an L2 evict-first policy, so that the 2 GiB streaming
+    // out of a large call leave the bit-stream words in L1 and L2
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     for (int32_t c0 = 0; c0 < C; c0 += KB) {
         uint32_t p[KB / 2];
 #pragma unroll
@@ -1902,14 +1907,18 @@ __device__ __forceinline__ uint32_t decode_symbols(DecState &st, const uint16_t 
             p[j >> 1] = pack(lo, symbol(j + 1));
         }
         if (KB == 16)
-            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+            asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], "
+                         "{%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
                          :
                          : "l"(orow + c0), "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]),
                            "r"(p[4 % (KB / 2)]), "r"(p[5 % (KB / 2)]), "r"(p[6 % (KB / 2)]),
-                           "r"(p[7 % (KB / 2)])
+                           "r"(p[7 % (KB / 2)]), "l"(pol)
                          : "memory");
         else
-            *reinterpret_cast<uint4 *>(orow + c0) = make_uint4(p[0], p[1], p[2], p[3]);
+            asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+                         :
+                         : "l"(orow + c0), "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "l"(pol)
+                         : "memory");
     }
     st.x = x;
     st.d = d;
