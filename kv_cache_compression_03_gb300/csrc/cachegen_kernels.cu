@@ -1718,7 +1718,8 @@ __device__ __forceinline__ float lds_f32(uint32_t a)
     return r;
 }
 
-// sb += inc when e <= T. `one` is 1 but comes from the kernel's arguments,
+// sb += inc when e <= T (sb: a search position, here the shared address of
+// the current entry). `one` is 1 but comes from the kernel's arguments,
 // so the predicated add compiles to a multiply-add on the FMA pipe and stays
 // off the integer ALU pipe, the decoder's busiest.
 __device__ __forceinline__ void probe_add(uint32_t &sb, uint32_t e, uint32_t T, uint32_t one,
