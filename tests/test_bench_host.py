@@ -61,3 +61,24 @@ def test_code_hash_ignores_comments_only():
     assert bench.code_hash(a) == bench.code_hash(b)
     assert bench.code_hash(a) != bench.code_hash(c)
 
+
+
+def test_recorded_counters_belong_to_the_current_kernel_source():
+    """profiles/traffic.json holds one-pass ncu counters of whole calls; the
+    bench reports them only while they match the kernel source they were
+    taken on. Every entry must carry the current source's hash, i.e. the
+    counters were taken again after the last change to the kernels."""
+    import json
+    with open(os.path.join(os.path.dirname(bench.KERNEL_SOURCE), "..", "..", "profiles",
+                           "traffic.json")) as f:
+        d = json.load(f)
+    sha = bench.kernel_source_hash()
+    entries = [(k, w, e) for k, v in d.items() if not k.startswith("_") for w, e in v.items()]
+    assert entries
+    for kernel, workload, e in entries:
+        assert e["source_sha"] == sha, (kernel, workload)
+        assert e["dram_bytes_per_launch"] > 0 and e["warp_instructions_per_launch"] > 0
+    for workload in ("llama8b_t16k", "glm4_9b_t32k"):
+        for kernel in ("k_encode_tiles", "k_decode_tiles"):
+            assert bench.recorded_counter(kernel, workload) == d[kernel][workload][
+                "dram_bytes_per_launch"]
