@@ -81,6 +81,7 @@ struct cg_bin_class {
 struct cg_side_stream {
     int device = -1;
     cudaStream_t stream = nullptr;
+    cudaStream_t stream_hi = nullptr;  // the same at the device's greatest priority
     cudaEvent_t fork = nullptr, join = nullptr;
     cudaError_t ensure();
     void release();
