@@ -189,6 +189,38 @@ def test_serialize_matches_oracle_container(orc):
     assert np.array_equal(_bits(out2), _bits(out))
 
 
+def test_container_copies_through_every_kind_of_host_buffer(orc):
+    """cg_serialize / cg_deserialize with pinned and pageable host buffers, at
+    offsets of 0, 4 and 1 bytes from an aligned start: every form gives the
+    oracle's container and decodes it back."""
+    name = "mistral7b_t1k"
+    p = synthetic.WORKLOADS[name]
+    bits = synthetic.generate(name, num_tokens=300)
+    k, v = synthetic.workload_specs(name)
+    L, _, T, C = bits.shape
+    codec, kv, enc, out = _run(bits, p["H"], p["D"], 256, k, v)
+    ref = orc.encode(bits, 256, k, v)
+    want = orc.serialize(ref, L, T, p["H"], p["D"], 256, k, v)
+    n = len(want)
+    pinned = torch.empty(n + 64, dtype=torch.uint8, pin_memory=True)
+    pageable = torch.empty(n + 64, dtype=torch.uint8)
+    for buf in (pinned, pageable):
+        for off in (0, 4, 1):
+            host = buf[off:off + n]
+            host.fill_(0xA5)
+            w = cg.cg_serialize(codec.plan, enc.bytestream, enc.lengths, enc.cdf, enc.amax,
+                                enc.stream_bytes, host)
+            assert w == n
+            assert bytes(host.numpy()) == want, (buf.is_pinned(), off)
+            enc2 = codec.alloc_encoded()
+            cg.cg_deserialize(codec.plan, host, enc2.bytestream, enc2.lengths, enc2.cdf,
+                              enc2.amax)
+            enc2.stream_bytes = enc.stream_bytes
+            out2 = codec.decode(enc2)
+            torch.cuda.synchronize()
+            assert np.array_equal(_bits(out2), _bits(out)), (buf.is_pinned(), off)
+
+
 def test_repeatable_and_side_stream(orc):
     name = "mistral7b_t1k"
     p = synthetic.WORKLOADS[name]
