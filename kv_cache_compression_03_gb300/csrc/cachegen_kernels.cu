@@ -10,8 +10,9 @@
 // K/V, layer). Tiles are grouped by bin count; each group is one launch of
 // a kernel specialised for 16 or 32 bins (or a generic one) with its own
 // shared-memory size and CTAs per SM, and the launches of one call run
-// concurrently on the caller's stream and a forked side stream. Encode
-// (then a tile scan and a pack):
+// concurrently on the caller's stream and a forked side stream (for the
+// encoder, one at the greatest priority, so its 32-bin tiles start first).
+// Encode (then a tile scan and a pack):
 //   A  16-bin rows counted four channels per thread whose row groups fill
 //      the block (1024 channels; 256 in four groups, ...): each thread loads
 //      its four channels of eight rows once (the next eight in flight), the
@@ -24,7 +25,9 @@
 //      warp reduction) and the row's scale factor; then a thread per four
 //      channels re-reads the block (L1/L2-resident), quantises, counts and
 //      writes the symbols (4-bit codes for 16 bins, else bytes). The next
-//      block's amax overlaps this block's counting.
+//      block's amax overlaps this block's counting. The last read of each
+//      raw row carries an L2 evict-first policy, so the streaming rows do
+//      not push the scratch out of L2 before phase C reads it back.
 //      Rows under 1024 channels are counted by row groups, each group into
 //      its own histogram copy (cg_count_layout); at <= 512 channels the
 //      maxima of all rows come first and the counting runs without block
@@ -44,7 +47,8 @@
 // one stream (a search of the CDF row against a per-symbol target, checked
 // against the coder's exact bounds; the bit buffer refilled once per
 // kRefillEvery symbols) and writes the dequantised bf16 row, 16 symbols per
-// 32-byte store where the rows allow it; calls with few tiles split each
+// 32-byte store where the rows allow it (no L1 allocation, L2 evict-first:
+// the output is not read again); calls with few tiles split each
 // tile's streams over four CTAs. A stream (or part) whose batch of symbols
 // over- or under-runs the 64-bit bit buffer (possible only for runs of a
 // group's rarest symbols) is redone on an exact path that checks after
