@@ -54,8 +54,11 @@
  *                16-byte aligned
  *     bytestream uint8, the concatenated streams, 16-byte aligned
  *
- * Threads: a plan holds a side stream and two events with which cg_encode
- * and cg_decode fork work onto a second stream and join it back. Calls that
+ * Threads: a plan holds two side streams and two events with which
+ * cg_encode and cg_decode fork work onto a second stream and join it back
+ * (cg_encode's side stream has the device's greatest stream priority, so
+ * its smaller bin-count classes, whose tiles take longer, are dispatched
+ * before the largest class and before lower-priority work). Calls that
  * use the same plan must therefore come from one host thread at a time (use
  * one plan per thread); calls on different plans are independent. Device
  * work of two calls may overlap only if they use different workspaces.
