@@ -650,16 +650,23 @@ def run_codec(args):
 
         e2e_step()
         torch.cuda.synchronize(dev)
-        barrier(world)
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            res = e2e_step()
-        torch.cuda.synchronize(dev)
-        t_e2e = aggregate_max(time.perf_counter() - t0, world, dev)
-        assert all(code == cg.CG_OK for code, _ in res)
+        # three timed runs of n_e2e steps; the figure is their median (the
+        # host link and the host's memory are shared with other tenants, and
+        # single runs have read far below the others)
+        runs = []
+        for _ in range(3):
+            barrier(world)
+            t0 = time.perf_counter()
+            for _ in range(n_e2e):
+                res = e2e_step()
+            torch.cuda.synchronize(dev)
+            t_e2e = aggregate_max(time.perf_counter() - t0, world, dev)
+            runs.append(world * raw * n_e2e / t_e2e / 1e9)
+            assert all(code == cg.CG_OK for code, _ in res)
         assert torch.equal(host_out.view(torch.int16), out.view(torch.int16).cpu())
         blob_bytes = sum(n for _, n in res)
-        e2e = {"value": round(world * raw * n_e2e / t_e2e / 1e9, 3), "unit": "GB/s",
+        e2e = {"value": round(sorted(runs)[1], 3), "unit": "GB/s",
+               "runs": [round(r, 3) for r in runs], "statistic": "median of 3 runs",
                "h2d_bytes_per_step": int(raw + blob_bytes),
                "d2h_bytes_per_step": int(blob_bytes + raw), "steps": n_e2e,
                "path": f"pinned host kv -> per {G}-layer group: H2D -> cg_encode -> "
